@@ -1,0 +1,394 @@
+// Oracle for fused LayerNorm / RMSNorm forward (optionally FP8-quantized) and
+// backward (optionally with a fused residual-gradient add).
+//
+// TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+// benchmark's CPU-baseline leg load this library.  The product path (the CUDA
+// library and its Python binding) never calls it, and this file shares no code,
+// header, table or helper with the CUDA sources.
+//
+// Plain, slow, single-threaded C++17.  Every quantity is computed in double from
+// the exact values of the stored inputs and rounded once into the stored dtype.
+// Sources followed (page titles as printed on the pages):
+//   [P1] "Implementation:NVIDIA TransformerEngine JAX XLA Normalization",
+//        sections Description and I/O Contract: LayerNorm/RMSNorm forward with
+//        mu (LayerNorm only) and rsigma saved for the backward pass, gamma,
+//        beta (LayerNorm only), zero_centered_gamma, epsilon, and FP8 output
+//        with delayed per-tensor scaling (scale, amax, scale_inv) or MXFP8
+//        block scaling, rowwise and optional columnwise.
+//   [P2] "Implementation:NVIDIA TransformerEngine Ops Fused Backward Add
+//        RMSNorm", sections Description and I/O Contract: grad_input is the
+//        RMSNorm input gradient plus the residual gradient; grad_weight is the
+//        gradient of the RMSNorm weight.
+//   [OCP-FP8] OCP 8-bit Floating Point Specification, E4M3 (bias 7, no
+//        infinities, NaN = S.1111.111, max normal 448, subnormals to 2^-9).
+//   [OCP-MX] OCP Microscaling Formats (MX) v1.0: E8M0 scale (bias 127,
+//        255 = NaN), shared exponent = floor(log2(block amax)) - emax_elem,
+//        emax_elem = 8 for E4M3, block size 32.
+// The pages do not write out the normalization formulas; the ones below are
+// the textbook definitions the page names refer to (biased two-pass variance,
+// eps inside the square root).  Parity of every function here is pinned by
+// the CPU tests (library routines in float64, finite differences, closed
+// forms, invariants and hand-derived format tables).
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+namespace {
+
+enum OrcDtype { ORC_F32 = 0, ORC_BF16 = 1, ORC_F16 = 2 };
+
+// ---- widening of stored values (exact) -------------------------------------
+
+double f32_bits_to_double(uint32_t b) {
+  float f;
+  std::memcpy(&f, &b, 4);
+  return static_cast<double>(f);
+}
+
+// IEEE binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits.
+double f16_bits_to_double(uint16_t h) {
+  const int sign = (h >> 15) & 1;
+  const int e = (h >> 10) & 0x1F;
+  const int m = h & 0x3FF;
+  double v;
+  if (e == 0) {
+    v = std::ldexp(static_cast<double>(m), -24);
+  } else if (e == 31) {
+    v = (m == 0) ? INFINITY : NAN;
+  } else {
+    v = std::ldexp(1.0 + m / 1024.0, e - 15);
+  }
+  return sign ? -v : v;
+}
+
+double load_elem(const void* p, int dt, int64_t i) {
+  switch (dt) {
+    case ORC_F32: {
+      uint32_t b;
+      std::memcpy(&b, static_cast<const uint8_t*>(p) + 4 * i, 4);
+      return f32_bits_to_double(b);
+    }
+    case ORC_BF16: {
+      uint16_t h;
+      std::memcpy(&h, static_cast<const uint8_t*>(p) + 2 * i, 2);
+      return f32_bits_to_double(static_cast<uint32_t>(h) << 16);
+    }
+    default: {
+      uint16_t h;
+      std::memcpy(&h, static_cast<const uint8_t*>(p) + 2 * i, 2);
+      return f16_bits_to_double(h);
+    }
+  }
+}
+
+// ---- rounding (round to nearest, ties to even) -----------------------------
+
+// Rounds v to a binary format with p significand bits (implicit bit included)
+// whose normal exponents start at emin.  Below 2^emin the quantum is fixed
+// (gradual underflow).  No overflow handling: the caller decides.
+double round_binary(double v, int p, int emin) {
+  if (v == 0.0 || !std::isfinite(v)) return v;
+  const double a = std::fabs(v);
+  int e2;
+  std::frexp(a, &e2);           // a = f * 2^e2, f in [0.5, 1)
+  int E = e2 - 1;               // a = 1.xxx * 2^E
+  if (E < emin) E = emin;
+  const double quantum = std::ldexp(1.0, E - p + 1);
+  const double r = std::nearbyint(a / quantum) * quantum;  // exact scaling
+  return v < 0 ? -r : r;
+}
+
+uint16_t double_to_bf16_bits(double v) {
+  if (std::isnan(v)) return 0x7FC0;
+  // bfloat16: 8 significand bits, emin -126, emax 127.
+  double r = round_binary(v, 8, -126);
+  const double maxf = std::ldexp(2.0 - std::ldexp(1.0, -7), 127);
+  if (std::fabs(r) > maxf) r = (r < 0) ? -INFINITY : INFINITY;
+  const float f = static_cast<float>(r);  // exact: r is representable
+  uint32_t b;
+  std::memcpy(&b, &f, 4);
+  return static_cast<uint16_t>(b >> 16);
+}
+
+uint16_t double_to_f16_bits(double v) {
+  if (std::isnan(v)) return 0x7E00;
+  // binary16: 11 significand bits, emin -14, emax 15.
+  double r = round_binary(v, 11, -14);
+  const uint16_t sign = std::signbit(r) ? 0x8000 : 0;
+  const double a = std::fabs(r);
+  const double maxf = std::ldexp(2.0 - std::ldexp(1.0, -10), 15);
+  if (a > maxf) return sign | 0x7C00;
+  if (a == 0.0) return sign;
+  if (a < std::ldexp(1.0, -14)) {
+    return sign | static_cast<uint16_t>(a / std::ldexp(1.0, -24));
+  }
+  int e2;
+  std::frexp(a, &e2);
+  const int E = e2 - 1;
+  const int m = static_cast<int>((a / std::ldexp(1.0, E) - 1.0) * 1024.0);
+  return sign | static_cast<uint16_t>(((E + 15) << 10) | m);
+}
+
+float double_to_f32(double v) { return static_cast<float>(v); }  // RNE conversion
+
+void store_elem(void* p, int dt, int64_t i, double v) {
+  uint8_t* b = static_cast<uint8_t*>(p);
+  switch (dt) {
+    case ORC_F32: {
+      const float f = double_to_f32(v);
+      std::memcpy(b + 4 * i, &f, 4);
+      break;
+    }
+    case ORC_BF16: {
+      const uint16_t h = double_to_bf16_bits(v);
+      std::memcpy(b + 2 * i, &h, 2);
+      break;
+    }
+    default: {
+      const uint16_t h = double_to_f16_bits(v);
+      std::memcpy(b + 2 * i, &h, 2);
+      break;
+    }
+  }
+}
+
+// ---- OCP FP8 E4M3 ----------------------------------------------------------
+
+// E4M3 encoding with round-to-nearest-even and saturation of finite (and
+// infinite) magnitudes above 448 to +-448; NaN maps to 0x7F.
+uint8_t e4m3_encode(double v) {
+  if (std::isnan(v)) return 0x7F;
+  const uint8_t sign = std::signbit(v) ? 0x80 : 0x00;
+  double a = std::fabs(v);
+  if (std::isinf(a)) return sign | 0x7E;
+  // 4 significand bits, normal exponents from -6; rounding first, then the
+  // saturation test (a rounded magnitude of 480 or more is not encodable).
+  a = round_binary(a, 4, -6);
+  if (a > 448.0) return sign | 0x7E;
+  if (a < std::ldexp(1.0, -6)) {
+    const int m = static_cast<int>(a / std::ldexp(1.0, -9));  // 0..7, exact
+    return sign | static_cast<uint8_t>(m);
+  }
+  int e2;
+  std::frexp(a, &e2);
+  const int E = e2 - 1;  // -6 .. 8
+  const int m = static_cast<int>((a / std::ldexp(1.0, E) - 1.0) * 8.0);
+  return sign | static_cast<uint8_t>(((E + 7) << 3) | m);
+}
+
+double e4m3_decode(uint8_t c) {
+  const int sign = (c >> 7) & 1;
+  const int e = (c >> 3) & 0xF;
+  const int m = c & 7;
+  double v;
+  if (e == 15 && m == 7) {
+    v = NAN;
+  } else if (e == 0) {
+    v = std::ldexp(static_cast<double>(m), -9);
+  } else {
+    v = std::ldexp(1.0 + m / 8.0, e - 7);
+  }
+  return sign ? -v : v;
+}
+
+// ---- OCP MX E8M0 shared scale ----------------------------------------------
+
+// Biased E8M0 code of the block scale 2^(floor(log2 A) - 8), A >= 0 being the
+// block amax held in fp32.  A = 0 gives code 0; A NaN/Inf gives 255 (NaN).
+uint8_t e8m0_code(float A) {
+  if (std::isnan(A) || std::isinf(A)) return 255;
+  if (A == 0.0f) return 0;
+  int e2;
+  std::frexp(static_cast<double>(A), &e2);  // exact, handles fp32 subnormals
+  const int floor_log2 = e2 - 1;
+  int c = floor_log2 - 8 + 127;
+  if (c < 0) c = 0;
+  if (c > 254) c = 254;
+  return static_cast<uint8_t>(c);
+}
+
+// Quantizes one element of a block whose scale code is c: the fp32 value of z
+// multiplied by 2^(127-c) (an exact power-of-two scaling) and encoded to E4M3.
+uint8_t mx_element(double z, uint8_t c) {
+  if (c == 255) return 0x7F;
+  const float z32 = static_cast<float>(z);
+  return e4m3_encode(std::ldexp(static_cast<double>(z32), 127 - static_cast<int>(c)));
+}
+
+}  // namespace
+
+extern "C" {
+
+// ---- format primitives (exported for the pins) ------------------------------
+
+uint8_t orc_e4m3_encode(double v) { return e4m3_encode(v); }
+double orc_e4m3_decode(uint8_t c) { return e4m3_decode(c); }
+uint8_t orc_e8m0_code(float a) { return e8m0_code(a); }
+uint16_t orc_bf16_bits(double v) { return double_to_bf16_bits(v); }
+uint16_t orc_f16_bits(double v) { return double_to_f16_bits(v); }
+double orc_widen(const void* p, int dt, int64_t i) { return load_elem(p, dt, i); }
+
+// Rounds n doubles into dtype dt (f32 / bf16 / f16), RNE.
+void orc_round(const double* v, int64_t n, int dt, void* out) {
+  for (int64_t i = 0; i < n; ++i) store_elem(out, dt, i, v[i]);
+}
+
+// ---- forward [P1 Description, I/O Contract] ---------------------------------
+//
+// For each row i (norm 0 = LayerNorm, 1 = RMSNorm):
+//   LayerNorm: mu = (1/H) sum_j x_ij;  var = (1/H) sum_j (x_ij - mu)^2
+//   RMSNorm:   var = (1/H) sum_j x_ij^2          (no mean)
+//   rsigma = 1 / sqrt(var + eps)
+//   g'_j = gamma_j, or 1 + gamma_j when zero_centered_gamma
+//   LayerNorm: z_ij = (x_ij - mu) * rsigma * g'_j + beta_j
+//   RMSNorm:   z_ij = x_ij * rsigma * g'_j
+// z, mu, rsigma are returned in double; mu may be NULL.  Returns 0.
+int orc_norm_fwd(const void* x, int in_dt, const void* gamma, const void* beta, int w_dt,
+                 int64_t rows, int64_t hidden, int norm, int zero_centered_gamma, double eps,
+                 double* z, double* mu, double* rsigma) {
+  std::vector<double> g(hidden), b(hidden, 0.0), xr(hidden);
+  for (int64_t j = 0; j < hidden; ++j) {
+    g[j] = load_elem(gamma, w_dt, j) + (zero_centered_gamma ? 1.0 : 0.0);
+    if (norm == 0 && beta != nullptr) b[j] = load_elem(beta, w_dt, j);
+  }
+  for (int64_t i = 0; i < rows; ++i) {
+    for (int64_t j = 0; j < hidden; ++j) xr[j] = load_elem(x, in_dt, i * hidden + j);
+    double m = 0.0;
+    if (norm == 0) {
+      double s = 0.0;
+      for (int64_t j = 0; j < hidden; ++j) s += xr[j];
+      m = s / static_cast<double>(hidden);
+    }
+    double ss = 0.0;
+    for (int64_t j = 0; j < hidden; ++j) {
+      const double d = xr[j] - m;
+      ss += d * d;
+    }
+    const double var = ss / static_cast<double>(hidden);
+    const double rs = 1.0 / std::sqrt(var + eps);
+    if (mu != nullptr) mu[i] = m;
+    rsigma[i] = rs;
+    for (int64_t j = 0; j < hidden; ++j) {
+      z[i * hidden + j] = (xr[j] - m) * rs * g[j] + b[j];
+    }
+  }
+  return 0;
+}
+
+// ---- FP8 delayed per-tensor scaling [P1 Description: scale/amax/scale_inv] --
+//
+// q = E4M3_satfinite_RNE(fp32(z) * scale), the product taken in fp32 (the
+// precision in which the value being quantized is held).  amax = max |z| over
+// all n values (NaN propagates), returned rounded to fp32.  scale_inv = 1/scale
+// rounded to fp32.
+void orc_quant_delayed(const double* z, int64_t n, float scale, uint8_t* q, float* amax,
+                       float* scale_inv) {
+  double a = 0.0;
+  bool any_nan = false;
+  for (int64_t i = 0; i < n; ++i) {
+    const double v = z[i];
+    if (std::isnan(v)) any_nan = true;
+    else if (std::fabs(v) > a) a = std::fabs(v);
+    const float z32 = static_cast<float>(v);
+    const float prod = static_cast<float>(static_cast<double>(z32) * static_cast<double>(scale));
+    q[i] = e4m3_encode(static_cast<double>(prod));
+  }
+  if (amax) *amax = any_nan ? NAN : static_cast<float>(a);
+  if (scale_inv) *scale_inv = static_cast<float>(1.0 / static_cast<double>(scale));
+}
+
+// ---- MXFP8 [P1 Description: "MXFP8 block" scaling; OCP-MX] ------------------
+//
+// Rowwise: blocks of 32 consecutive elements along hidden.  q [rows, hidden],
+// scales [rows, hidden/32].  hidden must be a multiple of 32.
+void orc_mxfp8_rowwise(const double* z, int64_t rows, int64_t hidden, uint8_t* q,
+                       uint8_t* scales) {
+  const int64_t nb = hidden / 32;
+  for (int64_t i = 0; i < rows; ++i) {
+    for (int64_t blk = 0; blk < nb; ++blk) {
+      const double* zb = z + i * hidden + blk * 32;
+      float A = 0.0f;
+      bool bad = false;
+      for (int k = 0; k < 32; ++k) {
+        const float a = std::fabs(static_cast<float>(zb[k]));
+        if (std::isnan(a)) bad = true;
+        else if (a > A) A = a;
+      }
+      const uint8_t c = bad ? 255 : e8m0_code(A);
+      scales[i * nb + blk] = c;
+      for (int k = 0; k < 32; ++k) q[i * hidden + blk * 32 + k] = mx_element(zb[k], c);
+    }
+  }
+}
+
+// Columnwise: blocks of 32 consecutive rows in one column.  q keeps the
+// [rows, hidden] layout; scales are [rows/32, hidden].  rows must be a
+// multiple of 32.
+void orc_mxfp8_colwise(const double* z, int64_t rows, int64_t hidden, uint8_t* q,
+                       uint8_t* scales) {
+  for (int64_t rb = 0; rb < rows / 32; ++rb) {
+    for (int64_t j = 0; j < hidden; ++j) {
+      float A = 0.0f;
+      bool bad = false;
+      for (int k = 0; k < 32; ++k) {
+        const float a = std::fabs(static_cast<float>(z[(rb * 32 + k) * hidden + j]));
+        if (std::isnan(a)) bad = true;
+        else if (a > A) A = a;
+      }
+      const uint8_t c = bad ? 255 : e8m0_code(A);
+      scales[rb * hidden + j] = c;
+      for (int k = 0; k < 32; ++k) {
+        const int64_t idx = (rb * 32 + k) * hidden + j;
+        q[idx] = mx_element(z[idx], c);
+      }
+    }
+  }
+}
+
+// ---- backward [P1 Description; P2 Description, I/O Contract] -----------------
+//
+// Given the saved fp32 mu (LayerNorm) and rsigma of each row:
+//   xhat = (x - mu) * rsigma   (LayerNorm)   or   x * rsigma   (RMSNorm)
+//   dy = dz * g'
+//   LayerNorm: dx = rsigma * (dy - mean_j(dy) - xhat * mean_j(dy * xhat))
+//   RMSNorm:   dx = rsigma * (dy - xhat * mean_j(dy * xhat))
+//   dx += dresidual when given (the fused residual-gradient add of [P2])
+//   dgamma_j = sum_i dz_ij * xhat_ij ;  dbeta_j = sum_i dz_ij  (LayerNorm)
+// dx [rows, hidden], dgamma [hidden], dbeta [hidden] (may be NULL) in double.
+int orc_norm_bwd(const void* dz, const void* x, int in_dt, const float* mu, const float* rsigma,
+                 const void* gamma, int w_dt, const void* dresidual, int64_t rows, int64_t hidden,
+                 int norm, int zero_centered_gamma, double* dx, double* dgamma, double* dbeta) {
+  std::vector<double> g(hidden), xh(hidden), dy(hidden), dzr(hidden);
+  for (int64_t j = 0; j < hidden; ++j) {
+    g[j] = load_elem(gamma, w_dt, j) + (zero_centered_gamma ? 1.0 : 0.0);
+    dgamma[j] = 0.0;
+    if (dbeta) dbeta[j] = 0.0;
+  }
+  for (int64_t i = 0; i < rows; ++i) {
+    const double m = (norm == 0) ? static_cast<double>(mu[i]) : 0.0;
+    const double rs = static_cast<double>(rsigma[i]);
+    double s_dy = 0.0, s_dyxh = 0.0;
+    for (int64_t j = 0; j < hidden; ++j) {
+      const double xv = load_elem(x, in_dt, i * hidden + j);
+      dzr[j] = load_elem(dz, in_dt, i * hidden + j);
+      xh[j] = (xv - m) * rs;
+      dy[j] = dzr[j] * g[j];
+      s_dy += dy[j];
+      s_dyxh += dy[j] * xh[j];
+    }
+    const double c1 = (norm == 0) ? s_dy / static_cast<double>(hidden) : 0.0;
+    const double c2 = s_dyxh / static_cast<double>(hidden);
+    for (int64_t j = 0; j < hidden; ++j) {
+      double d = rs * (dy[j] - c1 - xh[j] * c2);
+      if (dresidual) d += load_elem(dresidual, in_dt, i * hidden + j);
+      dx[i * hidden + j] = d;
+      dgamma[j] += dzr[j] * xh[j];
+      if (dbeta) dbeta[j] += dzr[j];
+    }
+  }
+  return 0;
+}
+
+}  // extern "C"

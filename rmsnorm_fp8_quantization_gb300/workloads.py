@@ -1,0 +1,117 @@
+"""Seeded synthetic workloads for the fused norm path.
+
+This module only draws random inputs; it holds none of the normalization or
+quantization arithmetic, so both the CUDA path and the CPU oracle can be fed
+from it without sharing any of the method's code.
+
+Draw order for every workload (one ``torch.Generator`` on the CPU, seeded):
+x, gamma, beta, dz, dresidual, then the structure (outlier channels, per-row
+magnitudes).  Each tensor is drawn in float32 and cast once to its stored
+dtype, so both sides see the same stored bytes.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import torch
+
+_DT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    norm: str                  # "layernorm" | "rmsnorm"
+    rows: int
+    hidden: int
+    in_dtype: str              # "f32" | "bf16" | "f16"
+    w_dtype: str
+    eps: float
+    scaling: str = "none"      # "none" | "delayed" | "mxfp8"
+    layout: str = "rowwise"    # "rowwise" | "colwise" | "rowwise_colwise"
+    zero_centered_gamma: bool = False
+    passes: tuple = ("fwd", "bwd")
+    x_mean: float = 0.0
+    x_std: float = 1.0
+    gamma_mean: float = 1.0    # gamma ~ gamma_mean + gamma_std * N(0,1)
+    gamma_std: float = 0.1
+    beta_std: float = 0.0      # LayerNorm beta ~ beta_std * N(0,1)
+    outlier_frac: float = 0.0  # fraction of channels multiplied by outlier_gain
+    outlier_gain: float = 1.0
+    row_log10_range: Optional[tuple] = None  # per-row magnitude 10^U(lo, hi)
+    dresidual: bool = False
+    amax_prev: float = 0.0     # delayed scaling: scale = 448 / amax_prev
+
+    def with_shape(self, rows: int, hidden: Optional[int] = None) -> "Workload":
+        return dataclasses.replace(self, rows=rows, hidden=self.hidden if hidden is None else hidden)
+
+
+WORKLOADS = {
+    # RMSNorm fwd+bwd, fp32 in/out/weights, 64 x 1024.
+    "rms_f32_64x1024": Workload(
+        "rms_f32_64x1024", "rmsnorm", 64, 1024, "f32", "f32", 1e-6),
+    # LayerNorm fwd+bwd, bf16 in/out, fp32 gamma/beta, 16384 x 4096.
+    "ln_bf16_16384x4096": Workload(
+        "ln_bf16_16384x4096", "layernorm", 16384, 4096, "bf16", "f32", 1e-5,
+        x_mean=0.5, x_std=2.0, beta_std=0.1),
+    # Same with a hidden size that is not a power of two.
+    "ln_bf16_16384x4000": Workload(
+        "ln_bf16_16384x4000", "layernorm", 16384, 4000, "bf16", "f32", 1e-5,
+        x_mean=0.5, x_std=2.0, beta_std=0.1),
+    # RMSNorm fwd bf16 -> E4M3, delayed per-tensor scaling, rowwise + transposed colwise.
+    "rms_bf16_e4m3_delayed_32768x8192": Workload(
+        "rms_bf16_e4m3_delayed_32768x8192", "rmsnorm", 32768, 8192, "bf16", "bf16", 1e-6,
+        scaling="delayed", layout="rowwise_colwise", passes=("fwd",),
+        outlier_frac=0.001, outlier_gain=20.0, amax_prev=30.0),
+    # RMSNorm fwd bf16 -> MXFP8 (1x32 rowwise, 32x1 colwise E8M0 scales), zero-centered gamma.
+    "rms_bf16_mxfp8_16384x5120": Workload(
+        "rms_bf16_mxfp8_16384x5120", "rmsnorm", 16384, 5120, "bf16", "bf16", 1e-6,
+        scaling="mxfp8", layout="rowwise_colwise", zero_centered_gamma=True, passes=("fwd",),
+        gamma_mean=0.0, gamma_std=0.05, row_log10_range=(-2.0, 2.0)),
+    # Fused backward-add RMSNorm, bf16 tensors, 32768 x 12288.
+    "rms_bwd_add_bf16_32768x12288": Workload(
+        "rms_bwd_add_bf16_32768x12288", "rmsnorm", 32768, 12288, "bf16", "bf16", 1e-6,
+        passes=("bwd",), dresidual=True),
+}
+
+
+def make_inputs(w: Workload, seed: int = 0) -> dict:
+    """Draws the workload's inputs as CPU tensors in their stored dtypes.
+
+    Keys: x, gamma, beta (LayerNorm, else None), dz, dresidual (or None),
+    scale (fp32 [1], delayed scaling, else None), amax (fp32 [1] previous
+    amax, delayed scaling, else None).
+    """
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    R, H = w.rows, w.hidden
+    x = torch.randn(R, H, generator=g, dtype=torch.float32) * w.x_std + w.x_mean
+    gamma = torch.randn(H, generator=g, dtype=torch.float32) * w.gamma_std + w.gamma_mean
+    beta = None
+    if w.norm == "layernorm":
+        beta = torch.randn(H, generator=g, dtype=torch.float32) * w.beta_std
+    dz = torch.randn(R, H, generator=g, dtype=torch.float32)
+    dres = torch.randn(R, H, generator=g, dtype=torch.float32) if w.dresidual else None
+    if w.outlier_frac > 0:
+        n_out = max(1, int(round(H * w.outlier_frac)))
+        ch = torch.randperm(H, generator=g)[:n_out]
+        x[:, ch] *= w.outlier_gain
+    if w.row_log10_range is not None:
+        lo, hi = w.row_log10_range
+        mag = torch.pow(10.0, torch.rand(R, generator=g, dtype=torch.float64) * (hi - lo) + lo)
+        x *= mag.to(torch.float32)[:, None]
+    it, wt = _DT[w.in_dtype], _DT[w.w_dtype]
+    out = {
+        "x": x.to(it),
+        "gamma": gamma.to(wt),
+        "beta": None if beta is None else beta.to(wt),
+        "dz": dz.to(it),
+        "dresidual": None if dres is None else dres.to(it),
+        "scale": None,
+        "amax": None,
+    }
+    if w.scaling == "delayed":
+        out["scale"] = torch.tensor([448.0 / w.amax_prev], dtype=torch.float32)
+        out["amax"] = torch.tensor([w.amax_prev], dtype=torch.float32)
+    return out
