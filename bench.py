@@ -1,0 +1,481 @@
+"""Benchmark of the fused norm hot path on GB300.
+
+One step = one pass of the whole path over one batch: the LayerNorm forward
+(bf16 in/out, fp32 gamma/beta, mu/rsigma saved) followed by the backward
+(dx, then dgamma/dbeta reduced over all rows), on 16384 rows x 4096.
+Inputs are resident in HBM when the timed region starts; L2 is flushed
+(a 512 MiB write) between timed steps, outside the timed events.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+instead (test infrastructure, single-threaded C++) on the same workload.
+Also reported, in ``detail``: every workload of the target table (forward and
+backward separately, GB/s against the HBM roofline).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+MAIN = "ln_bf16_16384x4096"
+METRIC = "norm fwd/bwd rows/s and achieved HBM GB/s (% of 8 TB/s) at bf16 h=4096-12288"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+ESZ = {"f32": 4, "bf16": 2, "f16": 2}
+
+
+# ---------------------------------------------------------------- algorithmic bytes
+
+def fwd_bytes(w) -> int:
+    """Each input read once, each output written once, weights counted once."""
+    N, H, e, we = w.rows, w.hidden, ESZ[w.in_dtype], ESZ[w.w_dtype]
+    b = N * H * e + H * we * (2 if w.norm == "layernorm" else 1)
+    b += N * 4 * (2 if w.norm == "layernorm" else 1)          # mu, rsigma
+    rowwise = w.scaling == "none" or w.layout != "colwise"
+    colwise = w.scaling != "none" and w.layout != "rowwise"
+    if w.scaling == "none":
+        b += N * H * e
+    else:
+        b += N * H * (int(rowwise) + int(colwise))
+        if w.scaling == "delayed":
+            b += 4 + 4 + 4 * (int(rowwise) + int(colwise))   # scale, amax, scale_inv(s)
+        else:
+            b += (N * H // 32) * (int(rowwise) + int(colwise))
+    return b
+
+
+def bwd_bytes(w) -> int:
+    N, H, e, we = w.rows, w.hidden, ESZ[w.in_dtype], ESZ[w.w_dtype]
+    streams = 3 + (1 if w.dresidual else 0)                     # dz, x, (dres), dx
+    b = streams * N * H * e + N * 4 * (2 if w.norm == "layernorm" else 1)
+    b += H * we + H * we * (2 if w.norm == "layernorm" else 1)  # gamma; dgamma (+dbeta)
+    return b
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- helpers
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        for k in ("hbm_gbs", "hbm_GBs", "hbm"):
+            if k in d:
+                v = d[k]
+                if isinstance(v, dict):
+                    v = v.get("burst", v.get("value"))
+                return float(v), "measured"
+    except (OSError, ValueError, TypeError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "rmsnorm_fp8_quantization_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, or
+    None if the kernel sources changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[kernel]
+        if e.get("source_hash") != kernel_source_hash():
+            return None
+        return e["dram_bytes_per_launch"]
+    except (OSError, ValueError, KeyError):
+        return None
+
+
+class L2Flush:
+    def __init__(self, dev):
+        self.buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def __call__(self):
+        self.buf.fill_(1)
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def make_step(ops, w, inp):
+    """Closures for the forward call, the backward call and their buffers."""
+    dev = inp["x"].device
+    outs = ops.fwd_outputs(w.rows, w.hidden, inp["x"].dtype, w.norm, w.scaling, w.layout, dev)
+    ws = ops.bwd_workspace(w.rows, w.hidden, inp["x"].dtype, inp["gamma"].dtype, w.norm,
+                           w.zero_centered_gamma, 0, dev)
+    dx = torch.empty_like(inp["x"])
+    dg = torch.empty_like(inp["gamma"])
+    db = torch.empty_like(inp["gamma"]) if w.norm == "layernorm" else None
+    rs = torch.rand(w.rows, device=dev) + 0.5
+    mu = torch.randn(w.rows, device=dev) * 0.1
+
+    def fwd():
+        ops.norm_fwd(inp["x"], inp["gamma"], inp["beta"], norm=w.norm, eps=w.eps,
+                     zero_centered_gamma=w.zero_centered_gamma, scaling=w.scaling,
+                     layout=w.layout, scale=inp["scale"], amax=inp["amax"], outputs=outs)
+
+    def bwd():
+        m = outs["mu"] if "fwd" in w.passes else mu
+        r = outs["rsigma"] if "fwd" in w.passes else rs
+        ops.norm_bwd(inp["dz"], inp["x"], m if w.norm == "layernorm" else None, r,
+                     inp["gamma"], inp["dresidual"], norm=w.norm,
+                     zero_centered_gamma=w.zero_centered_gamma, workspace=ws, dx=dx,
+                     dgamma=dg, dbeta=db)
+
+    return fwd, bwd, outs, (dx, dg, db)
+
+
+def time_calls(calls, steps, warmup, flush, barrier=None):
+    """Per step: flush L2, then time each call with events on the current
+    stream.  Returns (list of per-step ms per call, total ms)."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        for c in calls:
+            c()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    per = [[] for _ in calls]
+    tot = 0.0
+    for _ in range(steps):
+        flush()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+        ev[0].record(stream)
+        for i, c in enumerate(calls):
+            c()
+            ev[i + 1].record(stream)
+        ev[-1].synchronize()
+        for i in range(len(calls)):
+            per[i].append(ev[i].elapsed_time(ev[i + 1]))
+        tot += ev[0].elapsed_time(ev[-1])
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    return per, tot
+
+
+def run_gpu(args):
+    from rmsnorm_fp8_quantization_gb300 import _build
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if rank == 0:
+        _build.build()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        dist.barrier()
+        _build.build()  # no-op once rank 0 has built
+    else:
+        torch.cuda.set_device(0)
+    from rmsnorm_fp8_quantization_gb300 import ops
+    from rmsnorm_fp8_quantization_gb300.workloads import WORKLOADS, make_inputs
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    barrier = (lambda: dist.barrier()) if dist else None
+    flush = L2Flush(dev)
+    peak, peak_kind = measured_peak()
+
+    # ---- main workload: LayerNorm fwd + bwd
+    w = WORKLOADS[MAIN]
+    inp = make_inputs(w, seed=rank, device=str(dev))
+    fwd, bwd, outs, grads = make_step(ops, w, inp)
+    sampler = ClockSampler(dev.index)
+    with sampler:
+        per, tot = time_calls([fwd, bwd], args.steps, args.warmup, flush, barrier)
+    clocks = sampler.summary()
+    ms_step = tot / args.steps
+    if dist:
+        t = torch.tensor([tot], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot = float(t.item())
+    rows_total = w.rows * args.steps * world
+    value = rows_total / (tot / 1e3)
+    fwd_ms = statistics.mean(per[0])
+    bwd_ms = statistics.mean(per[1])
+    bb = bwd_bytes(w)
+    achieved = bb / (bwd_ms / 1e3) / 1e9
+
+    # ---- end to end through the C ABI with pinned host buffers
+    e2e = run_e2e(ops, w, inp, args, barrier, flush, world, dev)
+
+    detail = {}
+    if rank == 0 and not args.no_detail:
+        del inp, outs, grads
+        torch.cuda.empty_cache()
+        detail = run_detail(ops, WORKLOADS, make_inputs, args, flush, dev, peak)
+
+    result = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "rows/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": tot / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": MAIN, "rows": w.rows, "hidden": w.hidden, "norm": w.norm,
+                   "io_dtype": w.in_dtype, "w_dtype": w.w_dtype, "step": "fwd+bwd",
+                   "l2": "flushed (512 MiB write) between timed steps",
+                   "parallelism": f"replicas x{world}"},
+        "hbm_gbs": (fwd_bytes(w) + bb) / (ms_step / 1e3) / 1e9,
+        "fwd_ms": fwd_ms,
+        "bwd_ms": bwd_ms,
+        "roofline": {"bound": "hbm", "kernel": "norm_bwd (row pass + finalize)",
+                     "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": achieved / peak, "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
+                     "algorithmic_bytes_per_launch": bb,
+                     "traffic": recorded_traffic("bwd_row_kernel")},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+        "detail": detail,
+    }
+    if rank == 0:
+        result["cpu_baseline"] = cpu_baseline(args)
+        print(json.dumps(result))
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_e2e(ops, w, inp, args, barrier, flush, world, dev):
+    """Same step through the C ABI with host buffers: H2D of x, dz, gamma,
+    beta from pinned memory, forward, backward, D2H of out, mu, rsigma, dx,
+    dgamma, dbeta, all inside the timed region."""
+    host_in = {k: inp[k].cpu().pin_memory() for k in ("x", "dz", "gamma", "beta")}
+    dev_in = {k: torch.empty_like(inp[k]) for k in host_in}
+    dinp = dict(inp)
+    dinp.update(dev_in)
+    fwd, bwd, outs, (dx, dg, db) = make_step(ops, w, dinp)
+    res = [outs["out"], outs["mu"], outs["rsigma"], dx, dg, db]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in res]
+
+    def h2d():
+        for k in host_in:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+
+    def d2h():
+        for h, d in zip(host_out, res):
+            h.copy_(d, non_blocking=True)
+
+    steps = max(3, args.steps // 2)
+    _, tot = time_calls([h2d, fwd, bwd, d2h], steps, args.warmup, flush, barrier)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([tot], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot = float(t.item())
+    return {"value": w.rows * steps * world / (tot / 1e3), "unit": "rows/s",
+            "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host_in.values()),
+            "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out),
+            "ms_per_step": tot / steps}
+
+
+def run_detail(ops, WORKLOADS, make_inputs, args, flush, dev, peak):
+    out = {}
+    steps = max(5, args.steps // 2)
+    for name, w in WORKLOADS.items():
+        inp = make_inputs(w, seed=0, device=str(dev))
+        fwd, bwd, outs, grads = make_step(ops, w, inp)
+        calls, labels = [], []
+        if "fwd" in w.passes:
+            calls.append(fwd)
+            labels.append("fwd")
+        if "bwd" in w.passes:
+            calls.append(bwd)
+            labels.append("bwd")
+        per, _ = time_calls(calls, steps, 3, flush)
+        d = {}
+        for lab, ts in zip(labels, per):
+            ms = statistics.median(ts)
+            nb = fwd_bytes(w) if lab == "fwd" else bwd_bytes(w)
+            gbs = nb / (ms / 1e3) / 1e9
+            d[lab] = {"us": ms * 1e3, "rows_per_s": w.rows / (ms / 1e3), "bytes": nb,
+                      "gbs": gbs, "frac_of_peak": gbs / peak,
+                      "frac_of_8tbs": gbs / NOMINAL_HBM_GBS}
+        out[name] = d
+        del inp, outs, grads, fwd, bwd
+        torch.cuda.empty_cache()
+    return out
+
+
+# ---------------------------------------------------------------- CPU oracle arm
+
+def cpu_baseline(args, min_seconds=10.0):
+    """The oracle (single-threaded C++, double) on the main workload: full
+    forward + backward over all 16384 rows, repeated until >= 10 s of CPU
+    time; rows/s over all repetitions."""
+    import numpy as np
+
+    import oracle
+    from rmsnorm_fp8_quantization_gb300.workloads import WORKLOADS, make_inputs
+    w = WORKLOADS[MAIN]
+    inp = make_inputs(w, seed=0)
+    oracle.build()
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        z, mu, rs = oracle.norm_fwd(inp["x"], inp["gamma"], inp["beta"], 0, False, w.eps)
+        oracle.round_to(z, "bf16")
+        del z
+        dx, dg, db = oracle.norm_bwd(inp["dz"], inp["x"], mu.astype(np.float32),
+                                     rs.astype(np.float32), inp["gamma"], None, 0, False)
+        oracle.round_to(dx, "bf16")
+        del dx
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or reps >= 20:
+            break
+    return {"value": w.rows * reps / el, "unit": "rows/s", "cores": 1, "kind": "oracle",
+            "sample": f"full {w.rows}x{w.hidden} LayerNorm fwd+bwd, {reps} repetitions, "
+                      f"{el:.1f} s, single-threaded C++ (double)"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from rmsnorm_fp8_quantization_gb300.workloads import WORKLOADS
+    w = WORKLOADS[MAIN]
+    import numpy as np
+
+    import oracle
+    from rmsnorm_fp8_quantization_gb300.workloads import make_inputs
+    oracle.build()
+    # Each step: the oracle on a 1024-row sample of the workload (fwd + bwd).
+    sample = w.with_shape(1024)
+    inp = make_inputs(sample, seed=0)
+
+    def step():
+        z, mu, rs = oracle.norm_fwd(inp["x"], inp["gamma"], inp["beta"], 0, False, w.eps)
+        oracle.round_to(z, "bf16")
+        dx, _, _ = oracle.norm_bwd(inp["dz"], inp["x"], mu.astype(np.float32),
+                                   rs.astype(np.float32), inp["gamma"], None, 0, False)
+        oracle.round_to(dx, "bf16")
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    v = sample.rows * args.steps / el
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "rows/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": MAIN, "rows": w.rows, "hidden": w.hidden,
+                   "sample_rows_per_step": sample.rows},
+        "cpu_baseline": {"value": v, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{sample.rows} rows of {MAIN} per step (fwd+bwd)"},
+        "e2e": {"value": v, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gbnorm", choices=["gbnorm", "reference"])
+    ap.add_argument("--no-detail", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl != "reference":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

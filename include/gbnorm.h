@@ -1,0 +1,185 @@
+/*
+ * gbnorm — fused LayerNorm / RMSNorm forward and backward for GB300 (sm_103a).
+ *
+ * C ABI of libgbnorm.so.  The operations follow two pages:
+ *   "Implementation:NVIDIA TransformerEngine JAX XLA Normalization"
+ *     (sections Description, Signature, I/O Contract): the forward handler's
+ *     buffers (input, gamma, beta, scale, amax; output, colwise output, mu,
+ *     rsigma, scale_inv, colwise scale_inv, updated amax, workspace), its
+ *     attributes (norm type, scaling mode, quantize layout, zero-centered
+ *     gamma, epsilon, SM margin), the workspace-size queries and the backward
+ *     handler.
+ *   "Implementation:NVIDIA TransformerEngine Ops Fused Backward Add RMSNorm"
+ *     (sections Description, I/O Contract): the backward with the residual
+ *     gradient added to the input gradient in the same kernel.
+ *
+ * Arithmetic (x is one row of `hidden` elements; all device math in fp32):
+ *   LayerNorm: mu = mean(x); var = mean((x - mu)^2); rsigma = 1/sqrt(var + eps)
+ *              z = (x - mu) * rsigma * g' + beta
+ *   RMSNorm:   rsigma = 1/sqrt(mean(x^2) + eps);  z = x * rsigma * g'
+ *   g' = gamma, or 1 + gamma when zero_centered_gamma != 0.
+ *   Backward:  xhat = (x - mu) * rsigma (LayerNorm) or x * rsigma (RMSNorm),
+ *              dy = dz * g',
+ *              LayerNorm dx = rsigma * (dy - mean(dy) - xhat * mean(dy * xhat))
+ *              RMSNorm   dx = rsigma * (dy - xhat * mean(dy * xhat))
+ *              dx += dresidual when dresidual != NULL,
+ *              dgamma = sum over rows of dz * xhat, dbeta = sum over rows of dz.
+ *
+ * Conventions shared by every call:
+ *   - All tensor pointers are DEVICE pointers to contiguous row-major data
+ *     owned by the caller.  The library allocates nothing, keeps no state
+ *     between calls and never synchronizes: every operation (including the
+ *     cudaMemsetAsync of updated_amax) is enqueued on `stream`, so the calls
+ *     can be captured into a CUDA graph.
+ *   - A status is returned; nothing is thrown and nothing aborts.  Arguments
+ *     are validated before any work is enqueued; on an error nothing is
+ *     enqueued.  A launch failure is reported as GBN_ERR_CUDA.
+ *   - Buffers with a `rows` dimension may be NULL when rows == 0.
+ *   - Pointers that are not 16-byte aligned (or a hidden size that is not a
+ *     multiple of the 16-byte vector) are accepted and take a scalar path.
+ *   - SM margin: the persistent grids use (SM count - sm_margin) SMs, at
+ *     least one, times the kernel's occupancy.
+ *   - 1 <= hidden <= 2^24 and rows >= 0 (else GBN_ERR_SHAPE).  Rows that do
+ *     not fit the register-resident kernels (e.g. hidden > 65536 for bf16)
+ *     run on a slower generic kernel.
+ *   - Outputs must not alias inputs.
+ */
+#ifndef GBNORM_H_
+#define GBNORM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Norm type: the page's NVTE_Norm_Type (LayerNorm or RMSNorm). */
+typedef enum { GBN_LAYERNORM = 0, GBN_RMSNORM = 1 } gbn_norm_type;
+
+/* Scaling mode of the output (the page's JAXX_Scaling_Mode: no scaling,
+ * delayed per-tensor scaling, MXFP8 1D block scaling with 32 elements per
+ * E8M0 scale). */
+typedef enum {
+  GBN_SCALING_NONE = 0,
+  GBN_SCALING_DELAYED_TENSOR = 1,
+  GBN_SCALING_MXFP8_1D = 2
+} gbn_scaling_mode;
+
+/* Which quantized outputs are written (the page's JAXX_Quantize_Layout:
+ * rowwise, columnwise, or both).  Ignored when the scaling mode is NONE. */
+typedef enum {
+  GBN_LAYOUT_ROWWISE = 0,
+  GBN_LAYOUT_COLWISE = 1,
+  GBN_LAYOUT_ROWWISE_COLWISE = 2
+} gbn_quantize_layout;
+
+/* Element types.  Inputs and weights: F32, BF16, F16.  Unquantized output:
+ * the input type.  Quantized output: E4M3 (OCP FP8, 1 byte); MXFP8 scales:
+ * E8M0 (1 byte, bias 127). */
+typedef enum { GBN_F32 = 0, GBN_BF16 = 1, GBN_F16 = 2, GBN_E4M3 = 3, GBN_E8M0 = 4 } gbn_dtype;
+
+typedef enum {
+  GBN_OK = 0,
+  GBN_ERR_NULL = 1,      /* a pointer the chosen mode needs is NULL */
+  GBN_ERR_DTYPE = 2,     /* unsupported dtype or dtype combination */
+  GBN_ERR_SHAPE = 3,     /* rows/hidden out of range, or MXFP8 blocks do not tile */
+  GBN_ERR_ALIGNMENT = 4, /* reserved: misaligned pointers take the scalar path */
+  GBN_ERR_WORKSPACE = 5, /* workspace NULL or smaller than the queried size */
+  GBN_ERR_ENUM = 6,      /* norm type, scaling mode or layout out of range */
+  GBN_ERR_CUDA = 7       /* a CUDA runtime call or a launch failed */
+} gbn_status;
+
+/* Forward workspace size in bytes ("GetNormForwardWorkspaceSizes" on the
+ * first page).  The forward needs no workspace, so *bytes is set to 0 for
+ * every valid argument set; the call still validates its arguments.
+ * Returns GBN_ERR_NULL if bytes is NULL. */
+gbn_status gbn_norm_fwd_workspace_size(int64_t rows, int64_t hidden, gbn_dtype in_dtype,
+                                       gbn_dtype w_dtype, gbn_dtype out_dtype,
+                                       gbn_norm_type norm_type, gbn_scaling_mode scaling_mode,
+                                       gbn_quantize_layout quantize_layout,
+                                       int zero_centered_gamma, int sm_margin, int is_training,
+                                       size_t* bytes);
+
+/* Forward ("NormForwardFFI" on the first page).
+ *
+ *   x        [rows, hidden] in_dtype
+ *   gamma    [hidden] w_dtype
+ *   beta     [hidden] w_dtype, LayerNorm only (NULL for RMSNorm)
+ *   scale    fp32 [1], delayed scaling only: the multiplier applied before the
+ *            E4M3 cast (NULL otherwise)
+ *   amax     fp32 [1], delayed scaling: the previous amax.  Accepted for
+ *            interface parity and not read; updated_amax receives the fresh
+ *            amax of this call.  May be NULL.
+ *   out      rowwise output [rows, hidden]: in_dtype when the scaling mode is
+ *            NONE, else E4M3 codes.  Required unless the layout is COLWISE.
+ *   colwise_out  columnwise E4M3 output, required for COLWISE layouts:
+ *            delayed scaling: the transpose, [hidden, rows];
+ *            MXFP8: [rows, hidden] (not transposed), scaled per 32x1 block.
+ *   mu       fp32 [rows], LayerNorm only; may be NULL (not written)
+ *   rsigma   fp32 [rows]; may be NULL (not written)
+ *   scale_inv        delayed: fp32 [1] = 1/scale (rowwise layouts);
+ *                    MXFP8: E8M0 [rows, hidden/32] rowwise block scales
+ *   colwise_scale_inv  delayed: fp32 [1] = 1/scale (colwise layouts);
+ *                    MXFP8: E8M0 [rows/32, hidden] columnwise block scales
+ *   updated_amax     fp32 [1], delayed scaling: max |z| over the whole output
+ *                    (before scaling; NaN propagates).  Zeroed on `stream` by
+ *                    this call, then reduced into.
+ *   workspace        unused (the forward needs none); may be NULL.
+ *   eps      added to the variance inside the square root.
+ *
+ * MXFP8 needs hidden % 32 == 0, and rows % 32 == 0 for columnwise layouts
+ * (else GBN_ERR_SHAPE).  out_dtype must be in_dtype for NONE and GBN_E4M3
+ * otherwise (else GBN_ERR_DTYPE). */
+gbn_status gbn_norm_fwd(const void* x, const void* gamma, const void* beta, const float* scale,
+                        const float* amax, void* out, void* colwise_out, float* mu,
+                        float* rsigma, void* scale_inv, void* colwise_scale_inv,
+                        float* updated_amax, void* workspace, size_t workspace_bytes,
+                        int64_t rows, int64_t hidden, gbn_dtype in_dtype, gbn_dtype w_dtype,
+                        gbn_dtype out_dtype, gbn_norm_type norm_type,
+                        gbn_scaling_mode scaling_mode, gbn_quantize_layout quantize_layout,
+                        int zero_centered_gamma, float eps, int sm_margin, cudaStream_t stream);
+
+/* Backward workspace size in bytes ("GetNormBackwardWorkspaceSizes" on the
+ * first page): fp32 partial dgamma (and dbeta for LayerNorm) rows, one per
+ * CTA of the persistent grid.  Depends on the current device's SM count and
+ * occupancy, so query it on the device that will run the call.
+ * Returns GBN_ERR_CUDA if no device can be queried. */
+gbn_status gbn_norm_bwd_workspace_size(int64_t rows, int64_t hidden, gbn_dtype in_dtype,
+                                       gbn_dtype w_dtype, gbn_norm_type norm_type,
+                                       int zero_centered_gamma, int sm_margin, size_t* bytes);
+
+/* Backward (the first page's backward handler; with dresidual, the second
+ * page's fused backward-add).
+ *
+ *   dz, x      [rows, hidden] in_dtype
+ *   mu         fp32 [rows], LayerNorm only (NULL for RMSNorm)
+ *   rsigma     fp32 [rows]
+ *   gamma      [hidden] w_dtype
+ *   dresidual  [rows, hidden] in_dtype, or NULL for no add
+ *   dx         [rows, hidden] in_dtype
+ *   dgamma     [hidden] w_dtype
+ *   dbeta      [hidden] w_dtype, LayerNorm only (NULL for RMSNorm)
+ *   workspace  at least gbn_norm_bwd_workspace_size() bytes, 16-byte aligned
+ *              (GBN_ERR_WORKSPACE otherwise); its contents need no
+ *              initialization and are overwritten.
+ * Two kernels are enqueued: the row pass (dx and per-CTA partials) and a
+ * finalize pass that sums the partials in a fixed order (deterministic for a
+ * fixed device and sm_margin). */
+gbn_status gbn_norm_bwd(const void* dz, const void* x, const float* mu, const float* rsigma,
+                        const void* gamma, const void* dresidual, void* dx, void* dgamma,
+                        void* dbeta, void* workspace, size_t workspace_bytes, int64_t rows,
+                        int64_t hidden, gbn_dtype in_dtype, gbn_dtype w_dtype,
+                        gbn_norm_type norm_type, int zero_centered_gamma, int sm_margin,
+                        cudaStream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* gbn_status_string(gbn_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBNORM_H_ */

@@ -1,0 +1,335 @@
+// Device-side helpers: typed vector loads/stores, conversions, reductions,
+// FP8/E8M0 encoding through the hardware conversion, cluster primitives.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "gbn_internal.h"
+
+namespace gbn {
+
+// ---------------------------------------------------------------- raw loads
+
+// 16-byte streaming load: read-only path, no L1 allocation (the row is used
+// once by this CTA).
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// Cached read-only loads (weights: reused by every row of the CTA).
+__device__ __forceinline__ uint4 ld_cached16(const void* p) {
+  uint4 r;
+  asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint2 ld_cached8(const void* p) {
+  uint2 r;
+  asm("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+  return r;
+}
+
+// Fire-and-forget prefetch of a contiguous range into L2 by the bulk-copy
+// engine (address 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// ---------------------------------------------------------------- element types
+
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+  static constexpr int kDt = DT_F32;
+  __device__ __forceinline__ static float to_f(float v) { return v; }
+};
+template <> struct Elem<__nv_bfloat16> {
+  static constexpr int kDt = DT_BF16;
+  __device__ __forceinline__ static float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+};
+template <> struct Elem<__half> {
+  static constexpr int kDt = DT_F16;
+  __device__ __forceinline__ static float to_f(__half v) { return __half2float(v); }
+};
+
+// Unpacks 32-bit words holding packed elements of T into floats.
+template <typename T, int N>
+__device__ __forceinline__ void unpack(const uint32_t* w, float* f) {
+  if constexpr (sizeof(T) == 4) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) f[i] = __uint_as_float(w[i]);
+  } else if constexpr (Elem<T>::kDt == DT_BF16) {
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+      __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+      float2 v = __half22float2(h);
+      f[2 * i] = v.x;
+      f[2 * i + 1] = v.y;
+    }
+  }
+}
+
+// Packs floats into words of T, round to nearest even.
+template <typename T, int N>
+__device__ __forceinline__ void pack(const float* f, uint32_t* w) {
+  if constexpr (sizeof(T) == 4) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) w[i] = __float_as_uint(f[i]);
+  } else if constexpr (Elem<T>::kDt == DT_BF16) {
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+      __half2 h = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+  }
+}
+
+// Number of 32-bit words in a vector of VEC elements of T.
+template <typename T, int VEC>
+struct Words {
+  static constexpr int n = (VEC * (int)sizeof(T)) / 4;
+};
+
+// Loads VEC elements of T (16-byte aligned group) as raw words.
+template <typename T, int VEC, bool STREAM>
+__device__ __forceinline__ void ld_vec_raw(const T* p, uint32_t* w) {
+  constexpr int B = VEC * (int)sizeof(T);
+  static_assert(B % 8 == 0, "vector must be a multiple of 8 bytes");
+  if constexpr (B % 16 == 0) {
+#pragma unroll
+    for (int c = 0; c < B / 16; ++c) {
+      uint4 r = STREAM ? ld_stream16(reinterpret_cast<const uint8_t*>(p) + 16 * c)
+                       : ld_cached16(reinterpret_cast<const uint8_t*>(p) + 16 * c);
+      w[4 * c] = r.x; w[4 * c + 1] = r.y; w[4 * c + 2] = r.z; w[4 * c + 3] = r.w;
+    }
+  } else {
+    uint2 r = ld_cached8(p);
+    w[0] = r.x; w[1] = r.y;
+  }
+}
+
+// Loads VEC weights of runtime dtype `wdt` starting at element `idx` as floats.
+template <int VEC>
+__device__ __forceinline__ void ld_weights(const void* base, int wdt, int idx, float* f) {
+  if (wdt == DT_F32) {
+    uint32_t w[VEC];
+    ld_vec_raw<float, VEC, false>(reinterpret_cast<const float*>(base) + idx, w);
+    unpack<float, VEC>(w, f);
+  } else if (wdt == DT_BF16) {
+    uint32_t w[VEC / 2];
+    ld_vec_raw<__nv_bfloat16, VEC, false>(reinterpret_cast<const __nv_bfloat16*>(base) + idx, w);
+    unpack<__nv_bfloat16, VEC>(w, f);
+  } else {
+    uint32_t w[VEC / 2];
+    ld_vec_raw<__half, VEC, false>(reinterpret_cast<const __half*>(base) + idx, w);
+    unpack<__half, VEC>(w, f);
+  }
+}
+
+// Scalar element access for the generic (any alignment, any size) path.
+template <typename T>
+__device__ __forceinline__ float ld_scalar(const T* p, int64_t i) {
+  return Elem<T>::to_f(p[i]);
+}
+__device__ __forceinline__ float ld_weight_scalar(const void* base, int wdt, int64_t i) {
+  if (wdt == DT_F32) return reinterpret_cast<const float*>(base)[i];
+  if (wdt == DT_BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[i]);
+  return __half2float(reinterpret_cast<const __half*>(base)[i]);
+}
+template <typename T>
+__device__ __forceinline__ void st_scalar(T* p, int64_t i, float v);
+template <> __device__ __forceinline__ void st_scalar<float>(float* p, int64_t i, float v) {
+  p[i] = v;
+}
+template <>
+__device__ __forceinline__ void st_scalar<__nv_bfloat16>(__nv_bfloat16* p, int64_t i, float v) {
+  p[i] = __float2bfloat16_rn(v);
+}
+template <> __device__ __forceinline__ void st_scalar<__half>(__half* p, int64_t i, float v) {
+  p[i] = __float2half_rn(v);
+}
+__device__ __forceinline__ void st_weight_scalar(void* base, int wdt, int64_t i, float v) {
+  if (wdt == DT_F32) reinterpret_cast<float*>(base)[i] = v;
+  else if (wdt == DT_BF16) reinterpret_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(v);
+  else reinterpret_cast<__half*>(base)[i] = __float2half_rn(v);
+}
+
+// Stores a packed vector (16 or 32 bytes of words; 16-byte aligned).
+template <int NW>
+__device__ __forceinline__ void st_words(void* p, const uint32_t* w) {
+  static_assert(NW % 4 == 0 || NW == 2 || NW == 1, "");
+  if constexpr (NW % 4 == 0) {
+#pragma unroll
+    for (int c = 0; c < NW / 4; ++c)
+      reinterpret_cast<uint4*>(p)[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+  } else if constexpr (NW == 2) {
+    *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
+  } else {
+    *reinterpret_cast<uint32_t*>(p) = w[0];
+  }
+}
+
+// ---------------------------------------------------------------- FP8 / E8M0
+
+// Two floats to two E4M3 codes (hardware cvt, RNE, satfinite); `lo` lands in
+// the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  return static_cast<uint32_t>(
+      __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
+}
+__device__ __forceinline__ uint8_t e4m3(float v) {
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+}
+
+// Packs N (multiple of 4) E4M3 codes of v[i] * s into N/4 words.
+template <int N>
+__device__ __forceinline__ void e4m3_pack_scaled(const float* v, float s, uint32_t* w) {
+#pragma unroll
+  for (int i = 0; i < N / 4; ++i) {
+    const uint32_t a = e4m3x2(v[4 * i] * s, v[4 * i + 1] * s);
+    const uint32_t b = e4m3x2(v[4 * i + 2] * s, v[4 * i + 3] * s);
+    w[i] = a | (b << 16);
+  }
+}
+// Same with a per-element multiplier.
+template <int N>
+__device__ __forceinline__ void e4m3_pack_mul(const float* v, const float* s, uint32_t* w) {
+#pragma unroll
+  for (int i = 0; i < N / 4; ++i) {
+    const uint32_t a = e4m3x2(v[4 * i] * s[4 * i], v[4 * i + 1] * s[4 * i + 1]);
+    const uint32_t b = e4m3x2(v[4 * i + 2] * s[4 * i + 2], v[4 * i + 3] * s[4 * i + 3]);
+    w[i] = a | (b << 16);
+  }
+}
+
+// NaN-propagating maximum.
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// E8M0 code of the MX block scale for block amax A >= 0 (or NaN): the biased
+// exponent of 2^(floor(log2 A) - 8), 8 being the largest exponent of E4M3.
+// floor(log2 A) + 127 is A's exponent field for normal A; zero and subnormal
+// A clamp to code 0; Inf/NaN give 255.
+__device__ __forceinline__ uint32_t e8m0_code(float A) {
+  const uint32_t e = __float_as_uint(A) >> 23;  // sign is 0 for A >= 0
+  if (e >= 255u) return 255u;
+  return e > 8u ? e - 8u : 0u;
+}
+// 2^(127 - code) as fp32 (code <= 246 for finite fp32 A, so always normal);
+// NaN for code 255.
+__device__ __forceinline__ float e8m0_mult(uint32_t code) {
+  return code == 255u ? __uint_as_float(0x7FFFFFFFu) : __uint_as_float((254u - code) << 23);
+}
+
+// ---------------------------------------------------------------- reductions
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+__device__ __forceinline__ float2 warp_sum2(float2 v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    v.x += __shfl_xor_sync(0xFFFFFFFFu, v.x, o);
+    v.y += __shfl_xor_sync(0xFFFFFFFFu, v.y, o);
+  }
+  return v;
+}
+__device__ __forceinline__ float warp_max_nan(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmax_nan(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+// Block-wide sum; every thread gets the same bits.  `buf` holds 32 floats and
+// must alternate between two buffers on consecutive calls (one barrier per
+// call suffices then).
+__device__ __forceinline__ float block_sum(float v, float* buf, int lane, int warp, int nwarps) {
+  v = warp_sum(v);
+  if (nwarps == 1) return v;
+  if (lane == 0) buf[warp] = v;
+  __syncthreads();
+  float r = lane < nwarps ? buf[lane] : 0.f;
+  return warp_sum(r);
+}
+__device__ __forceinline__ float2 block_sum2(float2 v, float2* buf, int lane, int warp,
+                                             int nwarps) {
+  v = warp_sum2(v);
+  if (nwarps == 1) return v;
+  if (lane == 0) buf[warp] = v;
+  __syncthreads();
+  float2 r = lane < nwarps ? buf[lane] : make_float2(0.f, 0.f);
+  return warp_sum2(r);
+}
+
+// Final amax of a CTA into *amax (float bits as int: valid for values >= 0,
+// NaN compares above every finite value and Inf).  `buf` needs 32 floats and
+// must not be in use by other threads.
+__device__ __forceinline__ void block_amax_commit(float v, float* buf, float* amax) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = (blockDim.x + 31) >> 5;
+  v = warp_max_nan(v);
+  __syncthreads();
+  if (lane == 0) buf[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    float r = lane < nwarps ? buf[lane] : 0.f;
+    r = warp_max_nan(r);
+    if (lane == 0) atomicMax(reinterpret_cast<int*>(amax), static_cast<int>(__float_as_uint(r)));
+  }
+}
+
+// ---------------------------------------------------------------- clusters
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+// Barrier over every thread of every CTA in the cluster, with release /
+// acquire ordering of shared-memory writes (a hardware barrier, not a spin).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+// Reads a float2 from the shared memory of CTA `rank` of this cluster at the
+// address that `local` has in this CTA.
+__device__ __forceinline__ float2 dsmem_ld2(const float2* local, uint32_t rank) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(ra)
+               : "memory");
+  return v;
+}
+
+}  // namespace gbn

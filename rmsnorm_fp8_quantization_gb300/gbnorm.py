@@ -1,0 +1,132 @@
+"""ctypes binding of libgbnorm.so (the C ABI declared in include/gbnorm.h).
+
+Argument marshalling only: every function has the C name and argument order,
+takes torch tensors (device memory) or None for pointers and Python numbers
+for the scalars, and returns the integer status.  All computation happens in
+the library's CUDA kernels.  Importing fails loudly if the library has not
+been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgbnorm.so")
+
+# Enums of include/gbnorm.h.
+GBN_LAYERNORM, GBN_RMSNORM = 0, 1
+GBN_SCALING_NONE, GBN_SCALING_DELAYED_TENSOR, GBN_SCALING_MXFP8_1D = 0, 1, 2
+GBN_LAYOUT_ROWWISE, GBN_LAYOUT_COLWISE, GBN_LAYOUT_ROWWISE_COLWISE = 0, 1, 2
+GBN_F32, GBN_BF16, GBN_F16, GBN_E4M3, GBN_E8M0 = 0, 1, 2, 3, 4
+(GBN_OK, GBN_ERR_NULL, GBN_ERR_DTYPE, GBN_ERR_SHAPE, GBN_ERR_ALIGNMENT, GBN_ERR_WORKSPACE,
+ GBN_ERR_ENUM, GBN_ERR_CUDA) = range(8)
+
+TORCH_DTYPE = {torch.float32: GBN_F32, torch.bfloat16: GBN_BF16, torch.float16: GBN_F16}
+
+FUNCTIONS = ("gbn_norm_fwd_workspace_size", "gbn_norm_fwd", "gbn_norm_bwd_workspace_size",
+             "gbn_norm_bwd", "gbn_status_string")
+
+
+class GbnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {gbn_status_string(status)} ({status})")
+        self.status = status
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it first (python -m "
+            "rmsnorm_fp8_quantization_gb300._build); there is no fallback path")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I64, I, F, SZ = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float,
+                        ctypes.c_size_t)
+    lib.gbn_norm_fwd_workspace_size.argtypes = [I64, I64, I, I, I, I, I, I, I, I, I,
+                                                ctypes.POINTER(SZ)]
+    lib.gbn_norm_fwd_workspace_size.restype = I
+    lib.gbn_norm_fwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, I64, I64,
+                                 I, I, I, I, I, I, I, F, I, P]
+    lib.gbn_norm_fwd.restype = I
+    lib.gbn_norm_bwd_workspace_size.argtypes = [I64, I64, I, I, I, I, I, ctypes.POINTER(SZ)]
+    lib.gbn_norm_bwd_workspace_size.restype = I
+    lib.gbn_norm_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, SZ, I64, I64, I, I, I, I, I, P]
+    lib.gbn_norm_bwd.restype = I
+    lib.gbn_status_string.argtypes = [I]
+    lib.gbn_status_string.restype = ctypes.c_char_p
+    return lib
+
+
+_lib = _load()
+
+
+def library():
+    """The loaded ctypes.CDLL (for symbol checks)."""
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return ctypes.c_void_p(t)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def gbn_status_string(status: int) -> str:
+    return _lib.gbn_status_string(int(status)).decode()
+
+
+def gbn_norm_fwd_workspace_size(rows, hidden, in_dtype, w_dtype, out_dtype, norm_type,
+                                scaling_mode, quantize_layout, zero_centered_gamma, sm_margin,
+                                is_training):
+    """Returns (status, bytes)."""
+    n = ctypes.c_size_t(0)
+    st = _lib.gbn_norm_fwd_workspace_size(rows, hidden, in_dtype, w_dtype, out_dtype, norm_type,
+                                          scaling_mode, quantize_layout,
+                                          int(bool(zero_centered_gamma)), sm_margin,
+                                          int(bool(is_training)), ctypes.byref(n))
+    return st, n.value
+
+
+def gbn_norm_fwd(x, gamma, beta, scale, amax, out, colwise_out, mu, rsigma, scale_inv,
+                 colwise_scale_inv, updated_amax, workspace, workspace_bytes, rows, hidden,
+                 in_dtype, w_dtype, out_dtype, norm_type, scaling_mode, quantize_layout,
+                 zero_centered_gamma, eps, sm_margin, stream=None) -> int:
+    return _lib.gbn_norm_fwd(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(scale), _ptr(amax), _ptr(out),
+                             _ptr(colwise_out), _ptr(mu), _ptr(rsigma), _ptr(scale_inv),
+                             _ptr(colwise_scale_inv), _ptr(updated_amax), _ptr(workspace),
+                             workspace_bytes, rows, hidden, in_dtype, w_dtype, out_dtype,
+                             norm_type, scaling_mode, quantize_layout,
+                             int(bool(zero_centered_gamma)), float(eps), sm_margin,
+                             _stream(stream))
+
+
+def gbn_norm_bwd_workspace_size(rows, hidden, in_dtype, w_dtype, norm_type, zero_centered_gamma,
+                                sm_margin):
+    """Returns (status, bytes)."""
+    n = ctypes.c_size_t(0)
+    st = _lib.gbn_norm_bwd_workspace_size(rows, hidden, in_dtype, w_dtype, norm_type,
+                                          int(bool(zero_centered_gamma)), sm_margin,
+                                          ctypes.byref(n))
+    return st, n.value
+
+
+def gbn_norm_bwd(dz, x, mu, rsigma, gamma, dresidual, dx, dgamma, dbeta, workspace,
+                 workspace_bytes, rows, hidden, in_dtype, w_dtype, norm_type,
+                 zero_centered_gamma, sm_margin, stream=None) -> int:
+    return _lib.gbn_norm_bwd(_ptr(dz), _ptr(x), _ptr(mu), _ptr(rsigma), _ptr(gamma),
+                             _ptr(dresidual), _ptr(dx), _ptr(dgamma), _ptr(dbeta),
+                             _ptr(workspace), workspace_bytes, rows, hidden, in_dtype, w_dtype,
+                             norm_type, int(bool(zero_centered_gamma)), sm_margin,
+                             _stream(stream))

@@ -76,30 +76,40 @@ WORKLOADS = {
 }
 
 
-def make_inputs(w: Workload, seed: int = 0) -> dict:
-    """Draws the workload's inputs as CPU tensors in their stored dtypes.
+def make_inputs(w: Workload, seed: int = 0, device: str = "cpu") -> dict:
+    """Draws the workload's inputs in their stored dtypes on `device`.
+
+    The same seed gives the same values on every run on one device type; the
+    CPU and CUDA generators draw different streams.
 
     Keys: x, gamma, beta (LayerNorm, else None), dz, dresidual (or None),
     scale (fp32 [1], delayed scaling, else None), amax (fp32 [1] previous
     amax, delayed scaling, else None).
     """
-    g = torch.Generator(device="cpu")
+    g = torch.Generator(device=device)
     g.manual_seed(seed)
     R, H = w.rows, w.hidden
-    x = torch.randn(R, H, generator=g, dtype=torch.float32) * w.x_std + w.x_mean
-    gamma = torch.randn(H, generator=g, dtype=torch.float32) * w.gamma_std + w.gamma_mean
+    kw = dict(generator=g, dtype=torch.float32, device=device)
+
+    def draw(*shape):
+        t = torch.empty(*shape, dtype=torch.float32, device=device)
+        return t.normal_(generator=g)
+
+    x = draw(R, H).mul_(w.x_std).add_(w.x_mean)
+    gamma = draw(H).mul_(w.gamma_std).add_(w.gamma_mean)
     beta = None
     if w.norm == "layernorm":
-        beta = torch.randn(H, generator=g, dtype=torch.float32) * w.beta_std
-    dz = torch.randn(R, H, generator=g, dtype=torch.float32)
-    dres = torch.randn(R, H, generator=g, dtype=torch.float32) if w.dresidual else None
+        beta = draw(H).mul_(w.beta_std)
+    dz = draw(R, H)
+    dres = draw(R, H) if w.dresidual else None
     if w.outlier_frac > 0:
         n_out = max(1, int(round(H * w.outlier_frac)))
-        ch = torch.randperm(H, generator=g)[:n_out]
+        ch = torch.randperm(H, generator=g, device=device)[:n_out]
         x[:, ch] *= w.outlier_gain
     if w.row_log10_range is not None:
         lo, hi = w.row_log10_range
-        mag = torch.pow(10.0, torch.rand(R, generator=g, dtype=torch.float64) * (hi - lo) + lo)
+        u = torch.rand(R, **kw).to(torch.float64)
+        mag = torch.pow(10.0, u * (hi - lo) + lo)
         x *= mag.to(torch.float32)[:, None]
     it, wt = _DT[w.in_dtype], _DT[w.w_dtype]
     out = {
@@ -112,6 +122,6 @@ def make_inputs(w: Workload, seed: int = 0) -> dict:
         "amax": None,
     }
     if w.scaling == "delayed":
-        out["scale"] = torch.tensor([448.0 / w.amax_prev], dtype=torch.float32)
-        out["amax"] = torch.tensor([w.amax_prev], dtype=torch.float32)
+        out["scale"] = torch.tensor([448.0 / w.amax_prev], dtype=torch.float32, device=device)
+        out["amax"] = torch.tensor([w.amax_prev], dtype=torch.float32, device=device)
     return out

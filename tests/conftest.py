@@ -36,3 +36,15 @@ def orc():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def gpu():
+    """The built library's allocating wrappers, on a CUDA device."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from rmsnorm_fp8_quantization_gb300 import _build
+    _build.build()
+    from rmsnorm_fp8_quantization_gb300 import ops
+    return ops
