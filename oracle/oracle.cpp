@@ -271,7 +271,8 @@ int orc_norm_fwd(const void* x, int in_dt, const void* gamma, const void* beta, 
     if (mu != nullptr) mu[i] = m;
     rsigma[i] = rs;
     for (int64_t j = 0; j < hidden; ++j) {
-      z[i * hidden + j] = (xr[j] - m) * rs * g[j] + b[j];
+      // RMSNorm has no beta: nothing is added, so a zero product keeps its sign.
+      z[i * hidden + j] = norm == 0 ? (xr[j] - m) * rs * g[j] + b[j] : xr[j] * rs * g[j];
     }
   }
   return 0;
