@@ -461,6 +461,25 @@ def run_reference(args):
     }))
 
 
+def run_only(args):
+    """A short run of one workload's passes (the command profiled by ncu)."""
+    from rmsnorm_fp8_quantization_gb300 import _build
+    _build.build()
+    from rmsnorm_fp8_quantization_gb300 import ops
+    from rmsnorm_fp8_quantization_gb300.workloads import WORKLOADS, make_inputs
+    torch.cuda.set_device(0)
+    w = WORKLOADS[args.only]
+    if args.rows:
+        w = w.with_shape(args.rows)
+    inp = make_inputs(w, seed=0, device="cuda")
+    fwd, bwd, _, _ = make_step(ops, w, inp)
+    calls = [c for p, c in (("fwd", fwd), ("bwd", bwd)) if p in w.passes]
+    flush = L2Flush(torch.device("cuda"))
+    per, _ = time_calls(calls, args.steps, args.warmup, flush)
+    print(json.dumps({"workload": w.name, "rows": w.rows, "hidden": w.hidden,
+                      "us": [statistics.median(t) * 1e3 for t in per]}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -468,11 +487,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gbnorm", choices=["gbnorm", "reference"])
     ap.add_argument("--no-detail", action="store_true")
+    ap.add_argument("--only", default=None, help="time one workload's passes only")
+    ap.add_argument("--rows", type=int, default=0, help="with --only: override the row count")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl != "reference":
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.only:
+        run_only(args)
     else:
         run_gpu(args)
 

@@ -175,6 +175,16 @@ gbn_status gbn_norm_bwd(const void* dz, const void* x, const float* mu, const fl
                         gbn_norm_type norm_type, int zero_centered_gamma, int sm_margin,
                         cudaStream_t stream);
 
+/* Device-side error bits, sticky across calls on the current device:
+ *   bit 0 (GBN_DEVICE_ERR_COPY_TIMEOUT): a kernel waited longer than 2 s for
+ *   one of its own bulk copies into shared memory, stopped early and left
+ *   that call's outputs incomplete.
+ * Kernels never trap or spin without bound; this flag is how such a failure
+ * reaches the host.  The query synchronizes with the device.  With clear != 0
+ * the bits are reset after reading. */
+#define GBN_DEVICE_ERR_COPY_TIMEOUT 1u
+gbn_status gbn_device_error(unsigned int* flags, int clear);
+
 /* Human-readable name of a status code (static storage). */
 const char* gbn_status_string(gbn_status status);
 

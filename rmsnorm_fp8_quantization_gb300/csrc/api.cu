@@ -8,6 +8,9 @@
 // "Implementation:NVIDIA TransformerEngine Ops Fused Backward Add RMSNorm",
 // I/O Contract (the residual gradient added to grad_input).
 #include <cstdint>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "gbn_internal.h"
 #include "gbnorm.h"
@@ -17,6 +20,8 @@ namespace {
 using namespace gbn;
 
 constexpr int64_t kMaxHidden = int64_t(1) << 24;
+constexpr int kMaxRingStagesHost = 8;  // matches the kernels' mbarrier array
+constexpr int kMaxSmemPerCta = 220 * 1024;
 
 bool io_dtype(gbn_dtype d) { return d == GBN_F32 || d == GBN_BF16 || d == GBN_F16; }
 int esize(gbn_dtype d) { return d == GBN_F32 ? 4 : 2; }
@@ -28,56 +33,82 @@ const KernelTable& table(gbn_dtype in) {
   return kernels_f16();
 }
 
-// Vectors per thread and CTA size for a row of nvec 16-byte vectors.  Short
-// rows shrink the per-thread count so a warp stays busy; long rows grow it
-// until the CTA fits 1024 threads.  Returns false if even 8 do not fit.
-// `max_threads(nv)` is the largest CTA the kernel variant was compiled for.
+// Vectors per thread (NV) and CTA size for a row of nvec 16-byte vectors:
+// the first NV in {1, 2, 3, 4, 6, 8}, starting at `prefer_nv`, whose CTA
+// (nvec / NV threads, rounded up to a warp) fits max_threads(NV), the
+// largest CTA the kernel variant was compiled for; short rows take fewer
+// vectors per thread so that a warp stays busy.  False if none fits.
 bool row_geom(int64_t nvec, int vec, int prefer_nv, int (*max_threads)(int), RowGeom* g) {
-  int nv = prefer_nv;
-  while (nv > 1 && (nvec + nv - 1) / nv < 32) nv /= 2;
-  int64_t t = ((nvec + nv - 1) / nv + 31) / 32 * 32;
-  while (t > max_threads(nv) && nv < 8) {
-    nv *= 2;
-    t = ((nvec + nv - 1) / nv + 31) / 32 * 32;
+  static const int kNv[] = {1, 2, 3, 4, 6, 8};
+  for (int nv : kNv) {
+    if (nv < prefer_nv && nvec > 32 * nv) continue;
+    const int64_t t = ((nvec + nv - 1) / nv + 31) / 32 * 32;
+    if (t > max_threads(nv)) continue;
+    g->vec = vec;
+    g->nv = nv;
+    g->threads = static_cast<int>(t);
+    return true;
   }
-  if (t > max_threads(nv)) return false;
-  g->vec = vec;
-  g->nv = nv;
-  g->threads = static_cast<int>(t);
-  return true;
+  return false;
 }
 
 RowGeom generic_geom() { return RowGeom{1, 1, 256}; }
 
-int fwd_max_threads(int) { return 1024; }
+int fwd_ring_cap(int nv) { return fwd_ring_max_threads(nv); }
 int bwd_threads_cap(int nv) { return bwd_max_threads(nv); }
 
-// Cluster split of a 32-row stripe: the smallest cluster (<= 8 CTAs) whose
-// column slice gives every lane the same number (<= 4) of 16-byte vectors per
-// row; otherwise the smallest one with <= 4, then <= 8, per lane.
-bool stripe_geom(int64_t hidden, int vec, bool mxfp8, StripeGeom* g) {
-  for (int pass = 0; pass < 3; ++pass) {
-    for (int c = 1; c <= 8; ++c) {
-      if (hidden % c) continue;
-      const int64_t hc = hidden / c;
-      if (hc % vec) continue;
-      if (mxfp8 && hc % 32) continue;
-      if (hc % 8) continue;  // 4-column transpose groups and 8-byte code vectors
-      const int64_t nv_row = hc / vec;
-      const int64_t nvs = (nv_row + 31) / 32;
-      const bool exact = (nv_row % 32) == 0;
-      const int64_t cap = pass == 2 ? 8 : 4;
-      if (nvs > cap || (pass == 0 && !exact)) continue;
-      int t = 1;
-      while (t < nvs) t *= 2;
-      g->vec = vec;
-      g->nvs = t;
-      g->cluster = c;
-      g->hc = static_cast<int>(hc);
-      return true;
+// Cluster split of a 32-row stripe for the columnwise layouts.  Candidates:
+// C <= 8 CTAs per cluster, each taking hc = hidden / C columns (a multiple of
+// 8 and of the 16-byte vector; of 128 for MXFP8), at most 2048 two-byte or
+// 1024 four-byte columns, with the slice (or two, when they fit) in shared
+// memory.  Among them the one with the most co-resident CTAs (clusters x C;
+// packing differs per C, and small slices fit two CTAs per SM) wins; ties go
+// to two stages, then to the smaller cluster.  Cached per (device, dtype,
+// mode, hidden).
+bool stripe_geom(const KernelTable& kt, int in, int qm, bool ln, int64_t hidden, int esize,
+                 int sms, StripeGeom* out) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int, int, int64_t>, std::pair<bool, StripeGeom>> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const auto key = std::make_tuple(dev, in, qm, ln ? 1 : 0, hidden);
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+      *out = it->second.second;
+      return it->second.first;
     }
   }
-  return false;
+  const int vec = 16 / esize;
+  const int64_t hc_max = esize == 2 ? 2048 : 1024;
+  bool found = false;
+  StripeGeom best{};
+  int best_active = -1;
+  for (int c = 1; c <= 8; ++c) {
+    if (hidden % c) continue;
+    const int64_t hc = hidden / c;
+    // 16-byte vectors; MXFP8 row blocks of 32 = 8 lanes of 4 columns, in whole warps.
+    if (hc % vec || hc % 8 || (qm == Q_MXFP8 && hc % 128) || hc > hc_max) continue;
+    for (int stages = 2; stages >= 1; --stages) {
+      const int smem = stripe_smem_bytes(qm, ln, static_cast<int>(hc), esize, stages);
+      if (smem > kMaxSmemPerCta) continue;
+      StripeGeom g{c, static_cast<int>(hc), stages, smem, 0};
+      int n = 0;
+      if (kt.stripe_max_clusters(qm, ln, g, &n) != cudaSuccess || n < 1) continue;
+      const int active = n * c;  // co-resident CTAs
+      if (active > best_active) {  // strict: earlier (2 stages, smaller C) wins ties
+        best_active = active;
+        best = g;
+        best.max_clusters = n;
+        found = true;
+      }
+    }
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  cache[key] = std::make_pair(found, best);
+  *out = best;
+  return found;
 }
 
 gbn_status device_sms(int* sms) {
@@ -91,6 +122,56 @@ gbn_status device_sms(int* sms) {
 int effective_sms(int sms, int sm_margin) {
   const int e = sms - (sm_margin > 0 ? sm_margin : 0);
   return e < 1 ? 1 : e;
+}
+
+// ---- bulk-copy ring sizing
+
+
+// Stage count (1..max_stages) for the ring kernels: CTAs per SM (occupancy
+// with the ring's shared memory) times the stages being filled gives the
+// bytes in flight per SM.  Occupancy answers are cached per (device, kernel
+// choice).
+struct RingChoice {
+  int stages = 0;
+  int occ = 0;
+};
+
+template <typename OccFn>
+RingChoice choose_ring(int key_kind, int in, const RowGeom& g, int stage_bytes, int max_stages,
+                       OccFn occ_fn) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int, int, int, int>, RingChoice> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const auto key = std::make_tuple(dev, key_kind, in, g.nv, g.threads, stage_bytes);
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  // Bytes in flight per SM up to kRingTarget count first, then resident
+  // threads (latency hiding), then fewer stages.
+  constexpr int64_t kRingTarget = 128 * 1024;
+  RingChoice best;
+  int64_t best_inflight = -1;
+  int best_occ = 0;
+  for (int s = 1; s <= max_stages; ++s) {
+    const int smem = s * stage_bytes;
+    if (smem > kMaxSmemPerCta) break;
+    int occ = 0;
+    if (occ_fn(smem, &occ) != cudaSuccess || occ < 1) continue;
+    int64_t inflight = static_cast<int64_t>(occ) * (s > 1 ? s - 1 : 1) * stage_bytes;
+    if (inflight > kRingTarget) inflight = kRingTarget;
+    if (inflight > best_inflight || (inflight == best_inflight && occ > best_occ)) {
+      best_inflight = inflight;
+      best_occ = occ;
+      best.stages = s;
+      best.occ = occ;
+    }
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  cache[key] = best;
+  return best;
 }
 
 gbn_status check_fwd_args(int64_t rows, int64_t hidden, gbn_dtype in, gbn_dtype w, gbn_dtype out,
@@ -110,25 +191,44 @@ gbn_status check_fwd_args(int64_t rows, int64_t hidden, gbn_dtype in, gbn_dtype 
 
 struct BwdPlan {
   RowGeom geom;       // geometry of the vector path (or generic)
-  int parts;          // P: CTAs of the persistent grid = partial rows in the workspace
-  size_t ws_bytes;
+  int parts;          // P: upper bound on the CTAs of the persistent grid
+  size_t ws_bytes;    // P fp32 partial rows for dgamma (and dbeta)
 };
 
+// Ring choice of the backward row pass for geometry g (cached).
+RingChoice bwd_ring_choice(const KernelTable& kt, gbn_dtype in, bool ln, bool add,
+                           const RowGeom& g, int64_t hidden, int* stage_bytes) {
+  *stage_bytes = (add ? 3 : 2) * static_cast<int>((hidden * esize(in) + 127) / 128 * 128);
+  return choose_ring(20 + (ln ? 2 : 0) + (add ? 1 : 0), in, g, *stage_bytes, 4,
+                     [&](int smem, int* o) { return kt.bwd_ring_occupancy(ln, add, g, smem, o); });
+}
+
+// P, the partial rows of the workspace: the persistent grid of the ring
+// kernel (with or without the residual add, whichever is larger).  The
+// generic kernel, used for misaligned pointers, runs at most P CTAs too.
 gbn_status plan_bwd(int64_t rows, int64_t hidden, gbn_dtype in, gbn_norm_type norm,
                     int sm_margin, BwdPlan* plan) {
   int sms = 0;
   gbn_status st = device_sms(&sms);
   if (st != GBN_OK) return st;
   const int vec = 16 / esize(in);
+  const bool ln = norm == GBN_LAYERNORM;
   RowGeom g = generic_geom();
   if (hidden % vec != 0 || !row_geom(hidden / vec, vec, 2, bwd_threads_cap, &g)) g = generic_geom();
-  const bool ln = norm == GBN_LAYERNORM;
-  int occ_a = 0, occ_b = 0;
+  int occ = 0;
   const KernelTable& kt = table(in);
-  if (kt.bwd_occupancy(ln, false, g, &occ_a) != cudaSuccess) return GBN_ERR_CUDA;
-  if (kt.bwd_occupancy(ln, true, g, &occ_b) != cudaSuccess) return GBN_ERR_CUDA;
-  const int occ = occ_a > occ_b ? occ_a : occ_b;
-  int64_t parts = static_cast<int64_t>(effective_sms(sms, sm_margin)) * (occ > 0 ? occ : 1);
+  if (g.vec != 1) {
+    int sbytes = 0;
+    for (int add = 0; add < 2; ++add) {
+      const RingChoice rc = bwd_ring_choice(kt, in, ln, add != 0, g, hidden, &sbytes);
+      if (rc.stages >= 1 && rc.occ > occ) occ = rc.occ;
+    }
+  }
+  if (occ < 1) {
+    if (kt.bwd_generic_occupancy(&occ) != cudaSuccess) return GBN_ERR_CUDA;
+    if (occ < 1) occ = 1;
+  }
+  int64_t parts = static_cast<int64_t>(effective_sms(sms, sm_margin)) * occ;
   if (parts > rows) parts = rows;
   if (parts < 1) parts = 1;
   plan->geom = g;
@@ -242,24 +342,44 @@ gbn_status gbn_norm_fwd(const void* x, const void* gamma, const void* beta, cons
 
   if (colwise) {
     StripeGeom sg;
-    const bool stripe_ok = vec_ok && rows % 32 == 0 && aligned(colwise_out, 16) &&
-                           stripe_geom(hidden, vec, qm == Q_MXFP8, &sg);
+    const bool stripe_ok = vec_ok && rows % 32 == 0 && aligned(colwise_out, 32) &&
+                           (qm != Q_MXFP8 || aligned(colwise_scale_inv, 4)) &&
+                           stripe_geom(kt, in_dtype, qm, ln, hidden, esize(in_dtype), sms, &sg);
     if (stripe_ok) {
-      const cudaError_t e = kt.stripe_launch(qm, sg, p, static_cast<double>(esms) / sms, stream);
+      int64_t ncl = static_cast<int64_t>(static_cast<double>(sg.max_clusters) * esms / sms);
+      if (ncl > rows / 32) ncl = rows / 32;
+      if (ncl < 1) ncl = 1;
+      const cudaError_t e = kt.stripe_launch(qm, ln, sg, p, static_cast<int>(ncl), stream);
       return e == cudaSuccess ? GBN_OK : GBN_ERR_CUDA;
     }
     vec_ok = false;  // generic kernel writes every layout
   }
 
-  RowGeom g = generic_geom();
-  if (vec_ok && !row_geom(hidden / vec, vec, 4, fwd_max_threads, &g)) g = generic_geom();
+  RowGeom gr;
+  if (vec_ok && row_geom(hidden / vec, vec, 4, fwd_ring_cap, &gr)) {
+    // Rows streamed through a shared-memory ring by bulk copies.
+    const int stage_bytes = static_cast<int>((hidden * esize(in_dtype) + 127) / 128 * 128);
+    const int kind = qm * 2 + (ln ? 1 : 0);
+    const RingChoice rc = choose_ring(10 + kind, in_dtype, gr, stage_bytes, kMaxRingStagesHost,
+                                      [&](int smem, int* o) {
+                                        return kt.fwd_ring_occupancy(kind, gr, smem, o);
+                                      });
+    if (rc.stages >= 1) {
+      int64_t grid = static_cast<int64_t>(esms) * rc.occ;
+      if (grid > rows) grid = rows;
+      if (grid < 1) grid = 1;
+      const cudaError_t e = kt.fwd_ring_launch(kind, gr, rc.stages, rc.stages * stage_bytes, p,
+                                               static_cast<int>(grid), stream);
+      return e == cudaSuccess ? GBN_OK : GBN_ERR_CUDA;
+    }
+  }
+  // Generic kernel: persistent over 32-row stripes.
   int occ = 0;
-  if (kt.fwd_occupancy(qm, g, &occ) != cudaSuccess) return GBN_ERR_CUDA;
-  const int64_t units = g.vec == 1 ? (rows + 31) / 32 : rows;  // generic: 32-row stripes
+  if (kt.fwd_generic_occupancy(qm, &occ) != cudaSuccess) return GBN_ERR_CUDA;
   int64_t grid = static_cast<int64_t>(esms) * (occ > 0 ? occ : 1);
-  if (grid > units) grid = units;
+  if (grid > (rows + 31) / 32) grid = (rows + 31) / 32;
   if (grid < 1) grid = 1;
-  const cudaError_t e = kt.fwd_launch(qm, g, p, static_cast<int>(grid), stream);
+  const cudaError_t e = kt.fwd_generic_launch(qm, p, static_cast<int>(grid), stream);
   return e == cudaSuccess ? GBN_OK : GBN_ERR_CUDA;
 }
 
@@ -306,12 +426,20 @@ gbn_status gbn_norm_bwd(const void* dz, const void* x, const float* mu, const fl
   if (!vec_ok) g = generic_geom();
   const bool add = dresidual != nullptr;
   const KernelTable& kt = table(in_dtype);
-  int occ = 0;
-  if (kt.bwd_occupancy(ln, add, g, &occ) != cudaSuccess) return GBN_ERR_CUDA;
   int sms = 0;
   st = device_sms(&sms);
   if (st != GBN_OK) return st;
-  int64_t grid = static_cast<int64_t>(effective_sms(sms, sm_margin)) * (occ > 0 ? occ : 1);
+  const int esms = effective_sms(sms, sm_margin);
+  RingChoice rc;
+  int stage_bytes = 0;
+  if (g.vec != 1) rc = bwd_ring_choice(kt, in_dtype, ln, add, g, hidden, &stage_bytes);
+  int occ = rc.occ;
+  const bool ring = rc.stages >= 1;
+  if (!ring) {
+    g = generic_geom();
+    if (kt.bwd_generic_occupancy(&occ) != cudaSuccess) return GBN_ERR_CUDA;
+  }
+  int64_t grid = static_cast<int64_t>(esms) * (occ > 0 ? occ : 1);
   if (grid > plan.parts) grid = plan.parts;
   if (grid < 1) grid = 1;
 
@@ -331,8 +459,11 @@ gbn_status gbn_norm_bwd(const void* dz, const void* x, const float* mu, const fl
   p.norm = ln ? 0 : 1;
   p.zcg = zero_centered_gamma ? 1 : 0;
   p.w_dt = w_dtype == GBN_F32 ? DT_F32 : (w_dtype == GBN_BF16 ? DT_BF16 : DT_F16);
-  if (kt.bwd_launch(ln, add, g, p, static_cast<int>(grid), stream) != cudaSuccess)
-    return GBN_ERR_CUDA;
+  const cudaError_t le =
+      ring ? kt.bwd_ring_launch(ln, add, g, rc.stages, rc.stages * stage_bytes, p,
+                                static_cast<int>(grid), stream)
+           : kt.bwd_generic_launch(p, static_cast<int>(grid), stream);
+  if (le != cudaSuccess) return GBN_ERR_CUDA;
 
   FinalizeParams f = {};
   f.part_dgamma = p.part_dgamma;
@@ -343,6 +474,17 @@ gbn_status gbn_norm_bwd(const void* dz, const void* x, const float* mu, const fl
   f.hidden = static_cast<int>(hidden);
   f.w_dt = p.w_dt;
   return launch_bwd_finalize(f, stream) == cudaSuccess ? GBN_OK : GBN_ERR_CUDA;
+}
+
+gbn_status gbn_device_error(unsigned int* flags, int clear) {
+  if (!flags) return GBN_ERR_NULL;
+  unsigned int a = 0, b = 0, c = 0;
+  if (kernels_f32().read_device_error(&a, clear != 0) != cudaSuccess ||
+      kernels_bf16().read_device_error(&b, clear != 0) != cudaSuccess ||
+      kernels_f16().read_device_error(&c, clear != 0) != cudaSuccess)
+    return GBN_ERR_CUDA;
+  *flags = a | b | c;
+  return GBN_OK;
 }
 
 }  // extern "C"

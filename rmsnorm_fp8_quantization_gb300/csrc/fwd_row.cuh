@@ -1,5 +1,6 @@
-// Forward kernels for rowwise outputs: the vectorized row pass and the
-// generic (any size, any alignment, every layout) fallback.
+// Generic forward kernel: any size, any alignment, every layout.  The fast
+// paths are the ring kernels (ring.cuh) and the stripe kernel
+// (fwd_stripe.cuh).
 //
 // Operation: "Implementation:NVIDIA TransformerEngine JAX XLA Normalization",
 // Description and I/O Contract -- per row, mean (LayerNorm only) and rsigma,
@@ -12,154 +13,14 @@
 
 namespace gbn {
 
-// Row pass.  One CTA of T threads per row at a time, persistent over rows
-// (row = blockIdx.x + k * gridDim.x).  Thread t holds the NV vectors
-// v = k*T + t (VEC elements each, 16 bytes of input) of the row in registers,
-// so the row is read from HBM exactly once; gamma/beta come through L1.
-// The next row of this CTA is prefetched into L2 by the bulk-copy engine while
-// the current one is reduced.
-template <typename Tin, int QM, int NV>
-__global__ void __launch_bounds__(1024) fwd_row_kernel(const FwdParams p) {
-  constexpr int VEC = 16 / (int)sizeof(Tin);
-  constexpr int NW = Words<Tin, VEC>::n;  // 4 words per vector
-  __shared__ float red[2][32];
-  const int tid = threadIdx.x, T = blockDim.x;
-  const int lane = tid & 31, warp = tid >> 5, nwarps = T >> 5;
-  const int H = p.hidden;
-  const int nvec = H / VEC;
-  const bool ln = (p.norm == 0);
-  const float gadd = p.zcg ? 1.f : 0.f;
-  const float fH = static_cast<float>(H);
-  const uint32_t row_bytes = static_cast<uint32_t>(H) * sizeof(Tin);
-  float qscale = 1.f;
-  if constexpr (QM == Q_DELAYED) qscale = *p.scale;
-  float amax_t = 0.f;
-  int rb = 0;
-
-  for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
-    const Tin* xr = reinterpret_cast<const Tin*>(p.x) + row * H;
-    if (tid == 0 && row + gridDim.x < p.rows)
-      prefetch_l2(xr + static_cast<int64_t>(gridDim.x) * H, row_bytes);
-
-    uint32_t xw[NV][NW];
-#pragma unroll
-    for (int k = 0; k < NV; ++k) {
-      const int v = k * T + tid;
-      if (v < nvec) {
-        ld_vec_raw<Tin, VEC, true>(xr + v * VEC, xw[k]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < NW; ++i) xw[k][i] = 0u;
-      }
-    }
-
-    float mean = 0.f;
-    if (ln) {
-      float s = 0.f;
-#pragma unroll
-      for (int k = 0; k < NV; ++k) {
-        float f[VEC];
-        unpack<Tin, VEC>(xw[k], f);
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) s += f[e];
-      }
-      s = block_sum(s, red[rb], lane, warp, nwarps);
-      rb ^= 1;
-      mean = s / fH;
-    }
-    float ss = 0.f;
-#pragma unroll
-    for (int k = 0; k < NV; ++k) {
-      if (k * T + tid < nvec) {
-        float f[VEC];
-        unpack<Tin, VEC>(xw[k], f);
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-          const float d = f[e] - mean;
-          ss = fmaf(d, d, ss);
-        }
-      }
-    }
-    ss = block_sum(ss, red[rb], lane, warp, nwarps);
-    rb ^= 1;
-    const float rs = 1.f / sqrtf(ss / fH + p.eps);
-    if (tid == 0) {
-      if (ln && p.mu) p.mu[row] = mean;
-      if (p.rsigma) p.rsigma[row] = rs;
-    }
-
-#pragma unroll
-    for (int k = 0; k < NV; ++k) {
-      const int v = k * T + tid;
-      const bool act = v < nvec;
-      float z[VEC];
-      if (act) {
-        float f[VEC], g[VEC], b[VEC];
-        unpack<Tin, VEC>(xw[k], f);
-        ld_weights<VEC>(p.gamma, p.w_dt, v * VEC, g);
-        if (ln) {
-          ld_weights<VEC>(p.beta, p.w_dt, v * VEC, b);
-        } else {
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) b[e] = 0.f;
-        }
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) z[e] = (f[e] - mean) * rs * (g[e] + gadd) + b[e];
-      } else {
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) z[e] = 0.f;
-      }
-      const int64_t off = row * H + static_cast<int64_t>(v) * VEC;
-      if constexpr (QM == Q_NONE) {
-        if (act) {
-          uint32_t w[NW];
-          pack<Tin, VEC>(z, w);
-          st_words<NW>(reinterpret_cast<Tin*>(p.out) + off, w);
-        }
-      } else if constexpr (QM == Q_DELAYED) {
-        if (act) {
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) amax_t = fmax_nan(amax_t, fabsf(z[e]));
-          uint32_t w[VEC / 4];
-          e4m3_pack_scaled<VEC>(z, qscale, w);
-          st_words<VEC / 4>(reinterpret_cast<uint8_t*>(p.out) + off, w);
-        }
-      } else {  // MXFP8 rowwise: 32-element blocks span 32/VEC adjacent threads
-        constexpr int TPB = 32 / VEC;
-        float a = 0.f;
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) a = fmax_nan(a, fabsf(z[e]));
-#pragma unroll
-        for (int o = 1; o < TPB; o <<= 1) a = fmax_nan(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
-        if (act) {
-          const uint32_t c = e8m0_code(a);
-          uint32_t w[VEC / 4];
-          e4m3_pack_scaled<VEC>(z, e8m0_mult(c), w);
-          st_words<VEC / 4>(reinterpret_cast<uint8_t*>(p.out) + off, w);
-          if ((tid & (TPB - 1)) == 0) p.mx_scale[row * (H / 32) + (v * VEC) / 32] = static_cast<uint8_t>(c);
-        }
-      }
-    }
-  }
-
-  if constexpr (QM == Q_DELAYED) {
-    block_amax_commit(amax_t, red[0], p.amax);
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-      const float inv = 1.f / qscale;
-      if (p.scale_inv) *p.scale_inv = inv;
-      if (p.colwise_scale_inv) *p.colwise_scale_inv = inv;
-    }
-  }
-}
-
 // z of element (row, j) for the generic path.
 template <typename Tin>
 __device__ __forceinline__ float z_at(const FwdParams& p, int64_t row, int j, float mean, float rs,
                                       float gadd, bool ln) {
   const float x = ld_scalar(reinterpret_cast<const Tin*>(p.x), row * p.hidden + j);
   const float g = ld_weight_scalar(p.gamma, p.w_dt, j) + gadd;
-  const float b = ln ? ld_weight_scalar(p.beta, p.w_dt, j) : 0.f;
-  return (x - mean) * rs * g + b;
+  const float t = (x - mean) * rs;
+  return ln ? fmaf(t, g, ld_weight_scalar(p.beta, p.w_dt, j)) : t * g;
 }
 
 // Generic forward: any hidden size, any alignment, every layout.  One CTA of

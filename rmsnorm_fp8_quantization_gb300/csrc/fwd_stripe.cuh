@@ -7,278 +7,339 @@
 // tensors with scale/amax/scale_inv") and I/O Contract.
 //
 // A columnwise output needs 32 finished rows before any column can be
-// written, and 32 rows of a long row do not fit one SM.  So a thread-block
-// cluster of C CTAs takes one 32-row stripe: CTA `rank` owns columns
-// [rank*hc, (rank+1)*hc).  Each CTA loads its 32 x hc slice into registers
-// once, reduces per-row partial statistics, and exchanges them with the other
-// CTAs through distributed shared memory; the row statistics are combined in
-// the same fixed order in every CTA.  Rowwise codes go straight to HBM;
-// columnwise codes are staged in shared memory and written as 32-byte column
-// segments (delayed) or after a column-block amax pass (MXFP8).  x is read
-// from HBM exactly once.
+// written, and 32 rows of a long row do not fit one SM.  A thread-block
+// cluster of C CTAs therefore takes one 32-row stripe: CTA `rank` owns
+// columns [rank*hc, (rank+1)*hc).
+//   1. The CTA's 32 x hc slice arrives in shared memory by bulk copies (the
+//      next slice is prefetched into L2, and with two stages already copied,
+//      while this one is processed).
+//   2. One warp per four rows reduces the slice's per-row mean and M2; the 32
+//      pairs are pushed to every CTA of the cluster with `st.async`, whose
+//      bytes complete a transaction count on the receiver's mbarrier.  Every
+//      CTA merges the C partials of a row in rank order (identical results in
+//      all CTAs); no cluster-wide barrier per stripe.
+//   3. A thread item is 4 adjacent columns x all 32 rows, computed in packed
+//      fp32 pairs: rowwise codes go to HBM as 4-byte words (a warp writes 128
+//      contiguous bytes of a row); delayed codes are transposed in registers
+//      (4x4 byte transposes) and each column's 32 codes leave as one 32-byte
+//      store, a whole sector; MXFP8 row blocks reduce their amax over 8
+//      lanes, and each 32x1 column block lies inside one thread.
+// x is read from HBM once.
 #pragma once
 
-#include "gbn_device.cuh"
+#include "ring.cuh"
 
 namespace gbn {
 
-constexpr int kStripeRows = 32;
-constexpr int kStripeWarps = 8;
-constexpr int kRowsPerWarp = kStripeRows / kStripeWarps;  // 4 consecutive rows per warp
+constexpr int kStripeWarps = kStripeThreads / 32;
+constexpr int kRowsPerWarp = kStripeRows / kStripeWarps;  // 4
+constexpr int kMaxCluster = 8;
 
-// Dynamic shared memory bytes of the stripe kernel for a slice of hc columns.
-__host__ __device__ inline int stripe_smem_bytes(int qm, int hc) {
-  if (qm == Q_DELAYED) return kStripeRows * hc;  // codes tile [32][hc]
-  return (kStripeWarps + 1) * hc * 4;            // column partial maxima + multipliers
+// Pushes v into element `buf` of CTA `rank` of this cluster and reports
+// 8 bytes on that CTA's mbarrier `bar` (same offsets in every CTA).
+__device__ __forceinline__ void push_stat(float2* buf, uint64_t* bar, uint32_t rank, float2 v) {
+  uint32_t ra, rb;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(buf)), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_u32(bar)), "r"(rank));
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+               ::"r"(ra), "f"(v.x), "f"(v.y), "r"(rb)
+               : "memory");
 }
 
-template <typename Tin, int QM, int NVS>
-__global__ void __launch_bounds__(256, 1) fwd_stripe_kernel(const FwdParams p, const int hc) {
+// Four consecutive elements of a shared-memory row as two fp32 pairs.
+template <typename Tin>
+__device__ __forceinline__ void lds4_pairs(const Tin* p, uint64_t* pr) {
+  if constexpr (sizeof(Tin) == 4) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    widen_pairs<Tin, 4>(w, pr);
+  } else {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    const uint32_t w[2] = {u.x, u.y};
+    widen_pairs<Tin, 4>(w, pr);
+  }
+}
+
+// In-register 4x4 byte transpose: out[c] byte r = in[r] byte c.
+__device__ __forceinline__ void transpose4x4(const uint32_t* in, uint32_t* out) {
+  const uint32_t t0 = __byte_perm(in[0], in[1], 0x5140), t1 = __byte_perm(in[0], in[1], 0x7362);
+  const uint32_t t2 = __byte_perm(in[2], in[3], 0x5140), t3 = __byte_perm(in[2], in[3], 0x7362);
+  out[0] = __byte_perm(t0, t2, 0x5410);
+  out[1] = __byte_perm(t0, t2, 0x7632);
+  out[2] = __byte_perm(t1, t3, 0x5410);
+  out[3] = __byte_perm(t1, t3, 0x7632);
+}
+
+template <typename Tin, int QM, bool LN>
+__global__ void __launch_bounds__(kStripeThreads, 3)
+    fwd_stripe_kernel(const FwdParams p, const int hc, const int stages) {
   constexpr int VEC = 16 / (int)sizeof(Tin);
-  constexpr int NW = Words<Tin, VEC>::n;
-  constexpr int RPW = kRowsPerWarp;
-  extern __shared__ __align__(16) uint8_t smem[];
-  __shared__ float2 stat[2][kStripeRows];  // per row: (local mean, local M2) of this slice
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ uint64_t full[2];                          // x slice landed
+  __shared__ uint64_t statbar[2];                       // all C stat pushes landed
+  __shared__ float2 rbuf[2][kMaxCluster][kStripeRows];  // [stripe parity][sender][row]
+  __shared__ float2 mystat[kStripeRows];
+  __shared__ float2 rstat[kStripeRows];                 // (mean, rsigma) per row
   __shared__ float red[32];
+  __shared__ int s_abort;
+  __shared__ long long s_kfail;  // first stripe whose copy never landed
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t C = cluster_nctarank();
   const uint32_t rank = cluster_ctarank();
   const int H = p.hidden;
   const int c0 = static_cast<int>(rank) * hc;
-  const int nvs = hc / VEC;  // vectors per row in this slice
+  const int nvs = hc / VEC;
+  const int G = hc / 4;  // groups of 4 adjacent columns
   const int64_t N = p.rows;
   const int64_t nstripes = N / kStripeRows;
   const int64_t cid = blockIdx.x / C, ncl = gridDim.x / C;
-  const bool ln = (p.norm == 0);
-  const float gadd = p.zcg ? 1.f : 0.f;
-  const float fH = static_cast<float>(H), fhc = static_cast<float>(hc);
+  const int64_t count = cid < nstripes ? (nstripes - 1 - cid) / ncl + 1 : 0;
+  const float inv_h = 1.f / static_cast<float>(H), fhc = static_cast<float>(hc);
+  const uint32_t row_bytes = static_cast<uint32_t>(hc) * sizeof(Tin);
+  const uint32_t slice = kStripeRows * row_bytes;
+  const Tin* x = reinterpret_cast<const Tin*>(p.x);
+  uint8_t* xbuf = smem;
+  float* wg = reinterpret_cast<float*>(smem + stages * slice);  // g' [hc]
+  float* wb = wg + hc;                                          // beta [hc] (LayerNorm)
   float qscale = 1.f;
   if constexpr (QM == Q_DELAYED) qscale = *p.scale;
   float amax_t = 0.f;
-  const Tin* x = reinterpret_cast<const Tin*>(p.x);
-  int buf = 0;
 
-  for (int64_t s = cid; s < nstripes; s += ncl) {
-    const int64_t i0 = s * kStripeRows;
-    const int r0 = warp * RPW;  // first stripe row of this warp
-
-    // ---- load the warp's 4 rows of this CTA's slice
-    uint32_t xw[RPW][NVS][NW];
-#pragma unroll
-    for (int r = 0; r < RPW; ++r) {
-      const Tin* xr = x + (i0 + r0 + r) * H + c0;
-#pragma unroll
-      for (int j = 0; j < NVS; ++j) {
-        const int v = j * 32 + lane;
-        if (v < nvs) {
-          ld_vec_raw<Tin, VEC, true>(xr + v * VEC, xw[r][j]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < NW; ++i) xw[r][j][i] = 0u;
-        }
-      }
+  auto stripe_of = [&](int64_t k) { return cid + k * ncl; };
+  auto issue = [&](int b, int64_t k) {
+    const int64_t i0 = stripe_of(k) * kStripeRows;
+    mbar_arrive_expect_tx(&full[b], slice);
+    for (int r = 0; r < kStripeRows; ++r)
+      bulk_g2s(xbuf + b * slice + r * row_bytes, x + (i0 + r) * H + c0, row_bytes, &full[b]);
+  };
+  // Bounded waits by one thread, the rest of the CTA blocked on the barrier
+  // that follows (no spinning warps).  After the first timeout every later
+  // wait gives up at once and no further copies are issued (the outputs are
+  // then invalid and the device error flag is set).
+  auto wait = [&](uint64_t* bar, uint32_t parity, int64_t k) {
+    if (tid == 0 && !s_abort && !mbar_wait(bar, parity)) {
+      s_kfail = k;
+      s_abort = 1;
     }
-    if (lane < RPW && s + ncl < nstripes)
-      prefetch_l2(x + (i0 + ncl * kStripeRows + r0 + lane) * H + c0,
-                  static_cast<uint32_t>(hc * sizeof(Tin)));
+    __syncthreads();
+  };
 
-    // ---- per-row statistics of this slice (one warp owns whole row slices)
+  int64_t issued = 0;
+  if (tid == 0) {
+    s_abort = 0;
+    s_kfail = -1;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&statbar[i], 1);
+    }
+    fence_mbar_init();
+    for (; issued < stages && issued < count; ++issued) issue(static_cast<int>(issued), issued);
+  }
+  {
+    const float gadd = p.zcg ? 1.f : 0.f;
+    for (int c = tid; c < hc; c += kStripeThreads) {
+      wg[c] = ld_weight_scalar(p.gamma, p.w_dt, c0 + c) + gadd;
+      if constexpr (LN) wb[c] = ld_weight_scalar(p.beta, p.w_dt, c0 + c);
+    }
+  }
+  // Peers push statistics into this CTA's mbarriers: they must be initialized
+  // cluster-wide before the first push.
+  cluster_sync();
+
+  for (int64_t k = 0; k < count; ++k) {
+    const int64_t i0 = stripe_of(k) * kStripeRows;
+    const int b = stages == 2 ? static_cast<int>(k & 1) : 0;
+    const uint32_t par = static_cast<uint32_t>(stages == 2 ? (k >> 1) & 1 : k & 1);
+    const int sb = static_cast<int>(k & 1);  // stat buffer
+    if (tid < kStripeRows && k + stages < count)
+      prefetch_l2(x + (stripe_of(k + stages) * kStripeRows + tid) * H + c0, row_bytes);
+    if (tid == 0) mbar_arrive_expect_tx(&statbar[sb], C * kStripeRows * sizeof(float2));
+    wait(&full[b], par, k);
+    const Tin* xs = reinterpret_cast<const Tin*>(xbuf + b * slice);
+
+    // ---- 1. slice statistics, warp w owns rows 4w .. 4w+3
+    constexpr int NP = VEC / 2;
 #pragma unroll
-    for (int r = 0; r < RPW; ++r) {
+    for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+      const int r = warp * kRowsPerWarp + rr;
+      const uint4* xr = reinterpret_cast<const uint4*>(xs + r * hc);
       float m = 0.f;
-      if (ln) {
-        float sum = 0.f;
+      if constexpr (LN) {
+        uint64_t a = 0ull;
+        for (int v = lane; v < nvs; v += 32) {
+          const uint4 u = xr[v];
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+          uint64_t pr[NP];
+          widen_pairs<Tin, VEC>(w, pr);
 #pragma unroll
-        for (int j = 0; j < NVS; ++j) {
-          float f[VEC];
-          unpack<Tin, VEC>(xw[r][j], f);
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) sum += f[e];
+          for (int i = 0; i < NP; ++i) a = add2(a, pr[i]);
         }
-        m = warp_sum(sum) / fhc;
+        const float2 af = u2(a);
+        m = warp_sum(af.x + af.y) / fhc;
       }
-      float q = 0.f;
+      const uint64_t m2 = p2(m, m);
+      uint64_t q2 = 0ull;
+      for (int v = lane; v < nvs; v += 32) {
+        const uint4 u = xr[v];
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        uint64_t pr[NP];
+        widen_pairs<Tin, VEC>(w, pr);
 #pragma unroll
-      for (int j = 0; j < NVS; ++j) {
-        if (j * 32 + lane < nvs) {
-          float f[VEC];
-          unpack<Tin, VEC>(xw[r][j], f);
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) {
-            const float d = f[e] - m;
-            q = fmaf(d, d, q);
-          }
+        for (int i = 0; i < NP; ++i) {
+          const uint64_t d = LN ? sub2(pr[i], m2) : pr[i];
+          q2 = fma2(d, d, q2);
         }
       }
-      q = warp_sum(q);
-      if (lane == 0) stat[buf][r0 + r] = make_float2(m, q);
+      const float2 qf = u2(q2);
+      const float q = warp_sum(qf.x + qf.y);
+      if (lane == 0) mystat[r] = make_float2(m, q);
     }
-    cluster_sync();
-
-    // ---- combine the C slices of each row, in rank order (same in every CTA)
-    float mean[RPW], rs[RPW];
-#pragma unroll
-    for (int r = 0; r < RPW; ++r) {
-      float2 mine = make_float2(0.f, 0.f);
-      if (lane < static_cast<int>(C)) mine = dsmem_ld2(&stat[buf][r0 + r], lane);
-      float msum = 0.f, qsum = 0.f;
-      for (uint32_t c = 0; c < C; ++c) {
-        const float mc = __shfl_sync(0xFFFFFFFFu, mine.x, c);
-        msum += mc;
-      }
-      const float mu = ln ? msum / static_cast<float>(C) : 0.f;
-      for (uint32_t c = 0; c < C; ++c) {
-        const float mc = __shfl_sync(0xFFFFFFFFu, mine.x, c);
-        const float qc = __shfl_sync(0xFFFFFFFFu, mine.y, c);
-        const float d = mc - mu;
-        qsum += ln ? fmaf(fhc * d, d, qc) : qc;
-      }
-      mean[r] = mu;
-      rs[r] = 1.f / sqrtf(qsum / fH + p.eps);
-      if (rank == 0 && lane == 0) {
-        if (ln && p.mu) p.mu[i0 + r0 + r] = mu;
-        if (p.rsigma) p.rsigma[i0 + r0 + r] = rs[r];
-      }
+    __syncthreads();
+    if (warp == 0) {
+      for (uint32_t c = 0; c < C; ++c) push_stat(&rbuf[sb][rank][lane], &statbar[sb], c, mystat[lane]);
     }
-    buf ^= 1;
+    wait(&statbar[sb], static_cast<uint32_t>((k >> 1) & 1), -1);
 
-    // ---- normalize; rowwise codes to HBM, columnwise material to smem
-#pragma unroll
-    for (int j = 0; j < NVS; ++j) {
-      const int v = j * 32 + lane;
-      const bool act = v < nvs;
-      const int col = c0 + v * VEC;  // global column of element 0 of this vector
-      float g[VEC], b[VEC];
-      if (act) {
-        ld_weights<VEC>(p.gamma, p.w_dt, col, g);
-        if (ln) ld_weights<VEC>(p.beta, p.w_dt, col, b);
+    // ---- 2. merge the C partials of each row in rank order
+    if (warp == 0) {
+      const int r = lane;
+      float mu = 0.f, qsum = 0.f;
+      if constexpr (LN) {
+        float msum = 0.f;
+        for (uint32_t c = 0; c < C; ++c) msum += rbuf[sb][c][r].x;
+        mu = msum / static_cast<float>(C);
       }
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        if (!act) g[e] = 0.f;
-        if (!ln || !act) b[e] = 0.f;
-        g[e] += gadd;
+      for (uint32_t c = 0; c < C; ++c) {
+        const float2 v = rbuf[sb][c][r];
+        const float d = v.x - mu;
+        qsum += LN ? fmaf(fhc * d, d, v.y) : v.y;
       }
-      float cmax[VEC];
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) cmax[e] = 0.f;
-#pragma unroll
-      for (int r = 0; r < RPW; ++r) {
-        const int64_t row = i0 + r0 + r;
-        float f[VEC], z[VEC];
-        unpack<Tin, VEC>(xw[r][j], f);
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) z[e] = act ? (f[e] - mean[r]) * rs[r] * g[e] + b[e] : 0.f;
-        if constexpr (QM == Q_DELAYED) {
-          if (act) {
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) amax_t = fmax_nan(amax_t, fabsf(z[e]));
-            uint32_t w[VEC / 4];
-            e4m3_pack_scaled<VEC>(z, qscale, w);
-            if (p.write_rowwise) st_words<VEC / 4>(reinterpret_cast<uint8_t*>(p.out) + row * H + col, w);
-            st_words<VEC / 4>(smem + (r0 + r) * hc + v * VEC, w);  // colwise tile [32][hc]
-          }
-        } else {  // MXFP8
-          if (p.write_rowwise) {
-            constexpr int TPB = 32 / VEC;
-            float a = 0.f;
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) a = fmax_nan(a, fabsf(z[e]));
-#pragma unroll
-            for (int o = 1; o < TPB; o <<= 1) a = fmax_nan(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
-            if (act) {
-              const uint32_t c = e8m0_code(a);
-              uint32_t w[VEC / 4];
-              e4m3_pack_scaled<VEC>(z, e8m0_mult(c), w);
-              st_words<VEC / 4>(reinterpret_cast<uint8_t*>(p.out) + row * H + col, w);
-              if ((lane & (TPB - 1)) == 0) p.mx_scale[row * (H / 32) + col / 32] = static_cast<uint8_t>(c);
-            }
-          }
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) cmax[e] = fmax_nan(cmax[e], fabsf(z[e]));
-        }
-      }
-      if constexpr (QM == Q_MXFP8) {
-        if (act) {
-          float* colmax = reinterpret_cast<float*>(smem);  // [8 warps][hc]
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) colmax[warp * hc + v * VEC + e] = cmax[e];
-        }
+      const float rs = rsqrtf(fmaf(qsum, inv_h, p.eps));
+      rstat[r] = make_float2(mu, rs);
+      if (rank == 0) {
+        if (LN && p.mu) p.mu[i0 + r] = mu;
+        if (p.rsigma) p.rsigma[i0 + r] = rs;
       }
     }
     __syncthreads();
 
-    if constexpr (QM == Q_DELAYED) {
-      // ---- transposed write: thread takes 4 adjacent columns, 32 rows each
-      const uint32_t* tile = reinterpret_cast<const uint32_t*>(smem);
-      const int ngrp = hc / 4;
-      for (int cg = tid; cg < ngrp; cg += 256) {
+    // ---- 3. items of 4 columns x 32 rows
+    for (int cg = tid; cg < G; cg += kStripeThreads) {
+      const float4 g4 = reinterpret_cast<const float4*>(wg)[cg];
+      const uint64_t g01 = p2(g4.x, g4.y), g23 = p2(g4.z, g4.w);
+      uint64_t b01 = 0ull, b23 = 0ull;
+      if constexpr (LN) {
+        const float4 b4 = reinterpret_cast<const float4*>(wb)[cg];
+        b01 = p2(b4.x, b4.y);
+        b23 = p2(b4.z, b4.w);
+      }
+      const int col = c0 + 4 * cg;
+      const Tin* xcol = xs + 4 * cg;
+      // z of row r as two pairs
+      auto zrow = [&](int r, uint64_t& z01, uint64_t& z23) {
+        const float2 st = rstat[r];
+        const uint64_t m2 = p2(st.x, st.x), r2 = p2(st.y, st.y);
+        uint64_t xp[2];
+        lds4_pairs<Tin>(xcol + r * hc, xp);
+        const uint64_t t01 = mul2(LN ? sub2(xp[0], m2) : xp[0], r2);
+        const uint64_t t23 = mul2(LN ? sub2(xp[1], m2) : xp[1], r2);
+        z01 = LN ? fma2(t01, g01, b01) : mul2(t01, g01);
+        z23 = LN ? fma2(t23, g23, b23) : mul2(t23, g23);
+      };
+      auto absmax4 = [](uint64_t a, uint64_t b) {
+        const float2 x = u2(a), y = u2(b);
+        return fmax_nan(fmax_nan(fabsf(x.x), fabsf(x.y)), fmax_nan(fabsf(y.x), fabsf(y.y)));
+      };
+      uint8_t* orow = p.write_rowwise ? reinterpret_cast<uint8_t*>(p.out) + i0 * H + col : nullptr;
+      if constexpr (QM == Q_DELAYED) {
+        const uint64_t s2 = p2(qscale, qscale);
         uint32_t w[kStripeRows];
 #pragma unroll
-        for (int r = 0; r < kStripeRows; ++r) w[r] = tile[r * ngrp + cg];
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          const uint32_t sel = static_cast<uint32_t>(cc) | (static_cast<uint32_t>(cc + 4) << 4);
-          uint32_t o[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint32_t lo = __byte_perm(w[4 * q], w[4 * q + 1], sel);
-            const uint32_t hi = __byte_perm(w[4 * q + 2], w[4 * q + 3], sel);
-            o[q] = __byte_perm(lo, hi, 0x5410);
-          }
-          uint8_t* dst = p.colwise_out + static_cast<int64_t>(c0 + 4 * cg + cc) * N + i0;
-          st_words<8>(dst, o);
+        for (int r = 0; r < kStripeRows; ++r) {
+          uint64_t z01, z23;
+          zrow(r, z01, z23);
+          amax_t = fmax_nan(amax_t, absmax4(z01, z23));
+          w[r] = e4m3x4_pairs(z01, z23, s2);
+          if (p.write_rowwise) *reinterpret_cast<uint32_t*>(orow + static_cast<int64_t>(r) * H) = w[r];
         }
-      }
-    } else {
-      // ---- column-block scales, then columnwise codes
-      float* colmax = reinterpret_cast<float*>(smem);
-      float* colmul = colmax + kStripeWarps * hc;
-      for (int c = tid; c < hc; c += 256) {
-        float a = 0.f;
+        if (p.write_colwise) {
+          uint32_t o[4][8];  // [column][rows 4m..4m+3]
 #pragma unroll
-        for (int w = 0; w < kStripeWarps; ++w) a = fmax_nan(a, colmax[w * hc + c]);
-        const uint32_t code = e8m0_code(a);
-        colmul[c] = e8m0_mult(code);
-        p.mx_colwise_scale[s * H + c0 + c] = static_cast<uint8_t>(code);
-      }
-      __syncthreads();
+          for (int m = 0; m < 8; ++m) {
+            uint32_t t[4];
+            transpose4x4(&w[4 * m], t);
 #pragma unroll
-      for (int j = 0; j < NVS; ++j) {
-        const int v = j * 32 + lane;
-        if (v < nvs) {
-          const int col = c0 + v * VEC;
-          float g[VEC], b[VEC], m[VEC];
-          ld_weights<VEC>(p.gamma, p.w_dt, col, g);
-          if (ln) {
-            ld_weights<VEC>(p.beta, p.w_dt, col, b);
-          } else {
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) b[e] = 0.f;
+            for (int c = 0; c < 4; ++c) o[c][m] = t[c];
           }
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) {
-            g[e] += gadd;
-            m[e] = colmul[v * VEC + e];
+          for (int c = 0; c < 4; ++c)
+            st_global_v8(p.colwise_out + static_cast<int64_t>(col + c) * N + i0, o[c]);
+        }
+      } else {
+        // pass 1: rowwise MXFP8 (a 1x32 block is 8 lanes) and the column amax
+        float cm[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int r = 0; r < kStripeRows; ++r) {
+          uint64_t z01, z23;
+          zrow(r, z01, z23);
+          {
+            const float2 x = u2(z01), y = u2(z23);
+            cm[0] = fmax_nan(cm[0], fabsf(x.x));
+            cm[1] = fmax_nan(cm[1], fabsf(x.y));
+            cm[2] = fmax_nan(cm[2], fabsf(y.x));
+            cm[3] = fmax_nan(cm[3], fabsf(y.y));
           }
+          if (p.write_rowwise) {
+            float a = absmax4(z01, z23);
 #pragma unroll
-          for (int r = 0; r < RPW; ++r) {
-            float f[VEC], z[VEC];
-            unpack<Tin, VEC>(xw[r][j], f);
+            for (int o = 1; o < 8; o <<= 1) a = fmax_nan(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+            const uint32_t code = e8m0_code(a);
+            const float m = e8m0_mult(code);
+            *reinterpret_cast<uint32_t*>(orow + static_cast<int64_t>(r) * H) =
+                e4m3x4_pairs(z01, z23, p2(m, m));
+            if ((cg & 7) == 0)
+              p.mx_scale[(i0 + r) * (H / 32) + col / 32] = static_cast<uint8_t>(code);
+          }
+        }
+        // pass 2: 32x1 column blocks
+        if (p.write_colwise) {
+          uint32_t codes = 0;
+          float mul[4];
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) z[e] = (f[e] - mean[r]) * rs[r] * g[e] + b[e];
-            uint32_t w[VEC / 4];
-            e4m3_pack_mul<VEC>(z, m, w);
-            st_words<VEC / 4>(p.colwise_out + (i0 + r0 + r) * H + col, w);
+          for (int c = 0; c < 4; ++c) {
+            const uint32_t code = e8m0_code(cm[c]);
+            mul[c] = e8m0_mult(code);
+            codes |= code << (8 * c);
+          }
+          *reinterpret_cast<uint32_t*>(p.mx_colwise_scale + stripe_of(k) * H + col) = codes;
+          const uint64_t m01 = p2(mul[0], mul[1]), m23 = p2(mul[2], mul[3]);
+          uint8_t* crow = p.colwise_out + i0 * H + col;
+          for (int r = 0; r < kStripeRows; ++r) {
+            uint64_t z01, z23;
+            zrow(r, z01, z23);
+            const float2 x = u2(mul2(z01, m01)), y = u2(mul2(z23, m23));
+            *reinterpret_cast<uint32_t*>(crow + static_cast<int64_t>(r) * H) =
+                e4m3x2(x.x, x.y) | (e4m3x2(y.x, y.y) << 16);
           }
         }
       }
     }
-    // The next stripe's smem writes happen after its cluster barrier, which
-    // every thread of this CTA reaches only after finishing the reads above.
+    __syncthreads();
+    // Every thread is done with this stage and rstat.
+    if (tid == 0 && issued < count && !s_abort) {
+      issue(stages == 2 ? b : 0, issued);
+      ++issued;
+    }
   }
-  // Keep this CTA's shared memory alive until every peer has read its stats.
+
+  if (tid == 0 && s_abort) {
+    atomicOr(&g_gbn_device_error, 1u);
+    // Let copies still in flight land before this CTA's shared memory goes.
+    for (int64_t j = s_kfail < 0 ? issued : s_kfail; j < issued; ++j)
+      mbar_wait(&full[stages == 2 ? static_cast<int>(j & 1) : 0],
+                static_cast<uint32_t>(stages == 2 ? (j >> 1) & 1 : j & 1));
+  }
+  // No CTA leaves while a peer of its cluster may still push into it.
   cluster_sync();
 
   if constexpr (QM == Q_DELAYED) {

@@ -174,6 +174,13 @@ __device__ __forceinline__ void st_weight_scalar(void* base, int wdt, int64_t i,
   else reinterpret_cast<__half*>(base)[i] = __float2half_rn(v);
 }
 
+// 32-byte store (32-byte aligned): one full sector per instruction.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // Stores a packed vector (16 or 32 bytes of words; 16-byte aligned).
 template <int NW>
 __device__ __forceinline__ void st_words(void* p, const uint32_t* w) {
@@ -186,6 +193,91 @@ __device__ __forceinline__ void st_words(void* p, const uint32_t* w) {
     *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
   } else {
     *reinterpret_cast<uint32_t*>(p) = w[0];
+  }
+}
+
+// ---------------------------------------------------------------- packed fp32 pairs
+//
+// Blackwell executes two fp32 lanes per instruction (add/mul/fma .f32x2,
+// round to nearest even per lane, identical to the scalar forms).  A pair is
+// held as one 64-bit register pair: .x in the low half.
+
+__device__ __forceinline__ uint64_t p2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 u2(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// A 32-bit word of two packed elements of T as a pair of floats.
+template <typename T>
+__device__ __forceinline__ uint64_t widen2(uint32_t w) {
+  if constexpr (Elem<T>::kDt == DT_BF16) {
+    return p2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+  } else {
+    const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&w));
+    return p2(v.x, v.y);
+  }
+}
+// A pair of floats rounded (RNE) into one word of two packed elements of T.
+template <typename T>
+__device__ __forceinline__ uint32_t narrow2(uint64_t v) {
+  const float2 f = u2(v);
+  if constexpr (Elem<T>::kDt == DT_BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(f.x, f.y);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __half2 h = __floats2half2_rn(f.x, f.y);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+// N elements of T held in N/2 pairs, from raw words (N*sizeof(T)/4 words).
+template <typename T, int N>
+__device__ __forceinline__ void widen_pairs(const uint32_t* w, uint64_t* pr) {
+  if constexpr (sizeof(T) == 4) {
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) pr[i] = p2(__uint_as_float(w[2 * i]), __uint_as_float(w[2 * i + 1]));
+  } else {
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) pr[i] = widen2<T>(w[i]);
+  }
+}
+template <typename T, int N>
+__device__ __forceinline__ void narrow_pairs(const uint64_t* pr, uint32_t* w) {
+  if constexpr (sizeof(T) == 4) {
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+      const float2 f = u2(pr[i]);
+      w[2 * i] = __float_as_uint(f.x);
+      w[2 * i + 1] = __float_as_uint(f.y);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) w[i] = narrow2<T>(pr[i]);
   }
 }
 
@@ -220,6 +312,12 @@ __device__ __forceinline__ void e4m3_pack_mul(const float* v, const float* s, ui
     const uint32_t b = e4m3x2(v[4 * i + 2] * s[4 * i + 2], v[4 * i + 3] * s[4 * i + 3]);
     w[i] = a | (b << 16);
   }
+}
+
+// Four E4M3 codes of the pairs a = (v0, v1), b = (v2, v3), each scaled by s.
+__device__ __forceinline__ uint32_t e4m3x4_pairs(uint64_t a, uint64_t b, uint64_t s) {
+  const float2 x = u2(mul2(a, s)), y = u2(mul2(b, s));
+  return e4m3x2(x.x, x.y) | (e4m3x2(y.x, y.y) << 16);
 }
 
 // NaN-propagating maximum.
@@ -302,6 +400,68 @@ __device__ __forceinline__ void block_amax_commit(float v, float* buf, float* am
   }
 }
 
+// ---------------------------------------------------------------- bulk copies + mbarriers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+// Makes initialized mbarriers visible to the bulk-copy (async) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// Arrives once on `bar` and adds `bytes` to the transaction count of its
+// current phase.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+// Global -> shared bulk copy (16-byte aligned addresses, size a multiple of
+// 16) whose completion is reported as transactions on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+// One bounded wait for phase `parity`: the thread is suspended in hardware
+// until the phase completes or about `hint_ns` pass.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
+// Upper bound on any wait for this kernel's own bulk copies.  A copy that
+// has not landed after this long means something is wrong; the kernel then
+// records the fact in `err` and stops instead of spinning forever.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// Waits for phase `parity` of `bar` to complete; false after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity, 1000000u)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity, 1000000u)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
 // ---------------------------------------------------------------- clusters
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -329,6 +489,15 @@ __device__ __forceinline__ float2 dsmem_ld2(const float2* local, uint32_t rank) 
   float2 v;
   asm volatile("ld.shared::cluster.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(ra)
                : "memory");
+  return v;
+}
+
+__device__ __forceinline__ int dsmem_ld_int(const int* local, uint32_t rank) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(ra) : "memory");
   return v;
 }
 

@@ -65,41 +65,68 @@ struct FinalizeParams {
 
 // Launch geometry chosen by the host layer.
 struct RowGeom {
-  int vec;      // elements per vector: 16 bytes of the input type, or 1 (scalar path)
-  int nv;       // vectors per thread per row (1, 2, 4, 8)
+  int vec;      // elements per vector: 16 bytes of the input type, or 1 (generic path)
+  int nv;       // vectors per thread per row (1, 2, 3, 4, 6, 8)
   int threads;  // CTA size (multiple of 32, <= 1024)
 };
 
 struct StripeGeom {
-  int vec;      // as above
-  int nvs;      // vectors per lane per row slice (1, 2, 4, 8)
   int cluster;  // CTAs per cluster (1..8); each takes hidden/cluster columns
   int hc;       // columns per CTA
+  int stages;   // 32-row slices of x in shared memory (1 or 2)
+  int smem;     // dynamic shared memory bytes
+  int max_clusters;  // co-resident clusters of this geometry on the device
 };
 
 // Largest CTA of the backward row pass with NV vectors per thread: the
 // register budget per thread grows with NV (dgamma/dbeta partials live in
 // registers), so the CTA shrinks.
 constexpr int bwd_max_threads(int nv) {
-  return nv <= 1 ? 1024 : (nv == 2 ? 768 : (nv == 4 ? 512 : 256));
+  return nv <= 1 ? 1024 : nv <= 3 ? 512 : nv == 4 ? 384 : 256;
+}
+
+// Largest CTA of the forward ring kernel with NV vectors per thread.
+constexpr int fwd_ring_max_threads(int nv) {
+  return nv <= 1 ? 1024 : nv == 2 ? 768 : nv == 3 ? 640 : nv == 4 ? 512 : nv == 6 ? 384 : 256;
+}
+
+constexpr int kStripeRows = 32;
+constexpr int kStripeThreads = 256;
+
+// Dynamic shared memory of the stripe kernel: `stages` x 32-row slices of x,
+// then the CTA's weights (g' and, for LayerNorm, beta; fp32).
+inline int stripe_smem_bytes(int qm, bool ln, int hc, int esize, int stages) {
+  (void)qm;
+  return stages * kStripeRows * hc * esize + (ln ? 8 : 4) * hc;
 }
 
 // Launchers of one input dtype (one translation unit each).  Every function
 // returns the cudaError_t of the CUDA calls it made.
 struct KernelTable {
-  // Occupancy (CTAs per SM) of the rowwise forward variant for geometry g.
-  cudaError_t (*fwd_occupancy)(int qm, const RowGeom& g, int* blocks_per_sm);
-  // Rowwise forward (vectorized row pass, or the generic kernel when g.vec == 1;
-  // the generic kernel also writes every columnwise layout).
-  cudaError_t (*fwd_launch)(int qm, const RowGeom& g, const FwdParams& p, int grid,
-                            cudaStream_t stream);
+  // Occupancy (CTAs per SM) and launch of the generic forward kernel (any
+  // size and alignment, every layout; 256 threads per 32-row stripe).
+  cudaError_t (*fwd_generic_occupancy)(int qm, int* blocks_per_sm);
+  cudaError_t (*fwd_generic_launch)(int qm, const FwdParams& p, int grid, cudaStream_t stream);
   // Columnwise (and rowwise) forward over 32-row stripes split across a
-  // thread-block cluster; sm_fraction scales the co-resident cluster count.
-  cudaError_t (*stripe_launch)(int qm, const StripeGeom& g, const FwdParams& p,
-                               double sm_fraction, cudaStream_t stream);
-  cudaError_t (*bwd_occupancy)(bool layernorm, bool add, const RowGeom& g, int* blocks_per_sm);
-  cudaError_t (*bwd_launch)(bool layernorm, bool add, const RowGeom& g, const BwdParams& p,
-                            int grid, cudaStream_t stream);
+  // thread-block cluster of g.cluster CTAs, `clusters` of them (persistent).
+  cudaError_t (*stripe_max_clusters)(int qm, bool layernorm, const StripeGeom& g, int* clusters);
+  cudaError_t (*stripe_launch)(int qm, bool layernorm, const StripeGeom& g, const FwdParams& p,
+                               int clusters, cudaStream_t stream);
+  // Generic backward (any size and alignment, 256 threads).
+  cudaError_t (*bwd_generic_occupancy)(int* blocks_per_sm);
+  cudaError_t (*bwd_generic_launch)(const BwdParams& p, int grid, cudaStream_t stream);
+  // Ring variants (rows streamed through shared memory by bulk copies);
+  // `smem` = stages * stage bytes of dynamic shared memory.
+  // kind = qm * 2 + (LayerNorm ? 1 : 0)
+  cudaError_t (*fwd_ring_occupancy)(int kind, const RowGeom& g, int smem, int* blocks_per_sm);
+  cudaError_t (*fwd_ring_launch)(int kind, const RowGeom& g, int stages, int smem,
+                                 const FwdParams& p, int grid, cudaStream_t stream);
+  cudaError_t (*bwd_ring_occupancy)(bool layernorm, bool add, const RowGeom& g, int smem,
+                                    int* blocks_per_sm);
+  cudaError_t (*bwd_ring_launch)(bool layernorm, bool add, const RowGeom& g, int stages, int smem,
+                                 const BwdParams& p, int grid, cudaStream_t stream);
+  // Sticky device-side error bits of this translation unit's kernels.
+  cudaError_t (*read_device_error)(unsigned int* value, bool clear);
 };
 
 const KernelTable& kernels_f32();

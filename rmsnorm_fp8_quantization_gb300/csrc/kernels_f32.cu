@@ -5,8 +5,11 @@ namespace gbn {
 
 const KernelTable& kernels_f32() {
   using L = Launch<float>;
-  static const KernelTable table = {&L::fwd_occupancy, &L::fwd_launch, &L::stripe_launch,
-                                    &L::bwd_occupancy, &L::bwd_launch};
+  static const KernelTable table = {
+      &L::fwd_generic_occupancy, &L::fwd_generic_launch, &L::stripe_max_clusters, &L::stripe_launch,
+      &L::bwd_generic_occupancy, &L::bwd_generic_launch, &L::fwd_ring_occupancy,
+      &L::fwd_ring_launch,       &L::bwd_ring_occupancy, &L::bwd_ring_launch,
+      &L::read_device_error};
   return table;
 }
 

@@ -6,6 +6,7 @@
 #include "bwd.cuh"
 #include "fwd_row.cuh"
 #include "fwd_stripe.cuh"
+#include "ring.cuh"
 
 namespace gbn {
 
@@ -13,119 +14,160 @@ template <typename Tin>
 struct Launch {
   using Kfwd = void (*)(const FwdParams);
   using Kbwd = void (*)(const BwdParams);
-  using Kstripe = void (*)(const FwdParams, const int);
 
-  template <int QM>
-  static Kfwd fwd_row_kernel_for(const RowGeom& g) {
-    if (g.vec == 1) return fwd_generic_kernel<Tin, QM>;
-    switch (g.nv) {
-      case 1: return fwd_row_kernel<Tin, QM, 1>;
-      case 2: return fwd_row_kernel<Tin, QM, 2>;
-      case 4: return fwd_row_kernel<Tin, QM, 4>;
-      case 8: return fwd_row_kernel<Tin, QM, 8>;
-      default: return nullptr;
-    }
-  }
-  static Kfwd fwd_kernel(int qm, const RowGeom& g) {
-    switch (qm) {
-      case Q_NONE: return fwd_row_kernel_for<Q_NONE>(g);
-      case Q_DELAYED: return fwd_row_kernel_for<Q_DELAYED>(g);
-      case Q_MXFP8: return fwd_row_kernel_for<Q_MXFP8>(g);
-      default: return nullptr;
-    }
-  }
-
-  template <int QM>
-  static Kstripe stripe_kernel_for(int nvs) {
-    switch (nvs) {
-      case 1: return fwd_stripe_kernel<Tin, QM, 1>;
-      case 2: return fwd_stripe_kernel<Tin, QM, 2>;
-      case 4: return fwd_stripe_kernel<Tin, QM, 4>;
-      case 8: return fwd_stripe_kernel<Tin, QM, 8>;
-      default: return nullptr;
-    }
-  }
-  static Kstripe stripe_kernel(int qm, int nvs) {
-    if (qm == Q_DELAYED) return stripe_kernel_for<Q_DELAYED>(nvs);
-    if (qm == Q_MXFP8) return stripe_kernel_for<Q_MXFP8>(nvs);
+  static Kfwd fwd_generic(int qm) {
+    if (qm == Q_NONE) return fwd_generic_kernel<Tin, Q_NONE>;
+    if (qm == Q_DELAYED) return fwd_generic_kernel<Tin, Q_DELAYED>;
+    if (qm == Q_MXFP8) return fwd_generic_kernel<Tin, Q_MXFP8>;
     return nullptr;
   }
-
-  template <bool LN, bool ADD>
-  static Kbwd bwd_kernel_for(const RowGeom& g) {
-    if (g.vec == 1) return bwd_generic_kernel<Tin>;
-    switch (g.nv) {
-      case 1: return bwd_row_kernel<Tin, LN, ADD, 1>;
-      case 2: return bwd_row_kernel<Tin, LN, ADD, 2>;
-      case 4: return bwd_row_kernel<Tin, LN, ADD, 4>;
-      case 8: return bwd_row_kernel<Tin, LN, ADD, 8>;
-      default: return nullptr;
-    }
+  static cudaError_t fwd_generic_occupancy(int qm, int* occ) {
+    Kfwd k = fwd_generic(qm);
+    return k ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, k, 256, 0) : cudaErrorInvalidValue;
   }
-  static Kbwd bwd_kernel(bool ln, bool add, const RowGeom& g) {
-    if (ln) return add ? bwd_kernel_for<true, true>(g) : bwd_kernel_for<true, false>(g);
-    return add ? bwd_kernel_for<false, true>(g) : bwd_kernel_for<false, false>(g);
-  }
-
-  static cudaError_t fwd_occupancy(int qm, const RowGeom& g, int* occ) {
-    Kfwd k = fwd_kernel(qm, g);
+  static cudaError_t fwd_generic_launch(int qm, const FwdParams& p, int grid, cudaStream_t st) {
+    Kfwd k = fwd_generic(qm);
     if (!k) return cudaErrorInvalidValue;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, k, g.vec == 1 ? 256 : g.threads, 0);
+    k<<<grid, 256, 0, st>>>(p);
+    return cudaGetLastError();
   }
-  static cudaError_t fwd_launch(int qm, const RowGeom& g, const FwdParams& p, int grid,
-                                cudaStream_t st) {
-    Kfwd k = fwd_kernel(qm, g);
-    if (!k) return cudaErrorInvalidValue;
-    k<<<grid, g.vec == 1 ? 256 : g.threads, 0, st>>>(p);
+  static cudaError_t bwd_generic_occupancy(int* occ) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, bwd_generic_kernel<Tin>, 256, 0);
+  }
+  static cudaError_t bwd_generic_launch(const BwdParams& p, int grid, cudaStream_t st) {
+    bwd_generic_kernel<Tin><<<grid, 256, 0, st>>>(p);
     return cudaGetLastError();
   }
 
-  static cudaError_t stripe_launch(int qm, const StripeGeom& g, const FwdParams& p,
-                                   double sm_fraction, cudaStream_t st) {
-    Kstripe k = stripe_kernel(qm, g.nvs);
-    if (!k) return cudaErrorInvalidValue;
-    const int smem = stripe_smem_bytes(qm, g.hc);
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    const int64_t nstripes = p.rows / kStripeRows;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+  using Kstripe3 = void (*)(const FwdParams, const int, const int);
+  static Kstripe3 stripe_kernel(int qm, bool ln) {
+    if (qm == Q_DELAYED) return ln ? fwd_stripe_kernel<Tin, Q_DELAYED, true>
+                                   : fwd_stripe_kernel<Tin, Q_DELAYED, false>;
+    if (qm == Q_MXFP8) return ln ? fwd_stripe_kernel<Tin, Q_MXFP8, true>
+                                 : fwd_stripe_kernel<Tin, Q_MXFP8, false>;
+    return nullptr;
+  }
+  static void stripe_config(const StripeGeom& g, int nclusters, cudaLaunchConfig_t* cfg,
+                            cudaLaunchAttribute* attr) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(g.cluster);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(kStripeWarps * 32, 1, 1);
-    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-    cfg.stream = st;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    // Persistent grid: as many clusters as fit at once (scaled by the SM share
-    // left after sm_margin), never more than there are stripes.
-    cfg.gridDim = dim3(static_cast<unsigned>(g.cluster) * 152u, 1, 1);
-    int max_clusters = 0;
-    e = cudaOccupancyMaxActiveClusters(&max_clusters, k, &cfg);
+    *cfg = cudaLaunchConfig_t{};
+    cfg->gridDim = dim3(static_cast<unsigned>(nclusters * g.cluster), 1, 1);
+    cfg->blockDim = dim3(kStripeThreads, 1, 1);
+    cfg->dynamicSmemBytes = static_cast<size_t>(g.smem);
+    cfg->attrs = attr;
+    cfg->numAttrs = 1;
+  }
+  static cudaError_t stripe_max_clusters(int qm, bool ln, const StripeGeom& g, int* n) {
+    Kstripe3 k = stripe_kernel(qm, ln);
+    if (!k) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem);
     if (e != cudaSuccess) return e;
-    int64_t ncl = static_cast<int64_t>(max_clusters * sm_fraction);
-    if (ncl < 1) ncl = 1;
-    if (ncl > nstripes) ncl = nstripes > 0 ? nstripes : 1;
-    cfg.gridDim = dim3(static_cast<unsigned>(ncl * g.cluster), 1, 1);
-    e = cudaLaunchKernelEx(&cfg, k, p, g.hc);
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    stripe_config(g, 1024 / g.cluster, &cfg, attr);
+    return cudaOccupancyMaxActiveClusters(n, k, &cfg);
+  }
+  static cudaError_t stripe_launch(int qm, bool ln, const StripeGeom& g, const FwdParams& p,
+                                   int nclusters, cudaStream_t st) {
+    Kstripe3 k = stripe_kernel(qm, ln);
+    if (!k) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    stripe_config(g, nclusters, &cfg, attr);
+    cfg.stream = st;
+    e = cudaLaunchKernelEx(&cfg, k, p, g.hc, g.stages);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
 
-  static cudaError_t bwd_occupancy(bool ln, bool add, const RowGeom& g, int* occ) {
-    Kbwd k = bwd_kernel(ln, add, g);
-    if (!k) return cudaErrorInvalidValue;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, k, g.vec == 1 ? 256 : g.threads, 0);
+  // ---- bulk-copy ring variants
+  using Kring = void (*)(const FwdParams, const int);
+  using Kbring = void (*)(const BwdParams, const int);
+
+  template <int QM, bool LN>
+  static Kring fwd_ring_for(int nv) {
+    switch (nv) {
+      case 1: return fwd_ring_kernel<Tin, QM, LN, 1>;
+      case 2: return fwd_ring_kernel<Tin, QM, LN, 2>;
+      case 3: return fwd_ring_kernel<Tin, QM, LN, 3>;
+      case 4: return fwd_ring_kernel<Tin, QM, LN, 4>;
+      case 6: return fwd_ring_kernel<Tin, QM, LN, 6>;
+      case 8: return fwd_ring_kernel<Tin, QM, LN, 8>;
+      default: return nullptr;
+    }
   }
-  static cudaError_t bwd_launch(bool ln, bool add, const RowGeom& g, const BwdParams& p, int grid,
-                                cudaStream_t st) {
-    Kbwd k = bwd_kernel(ln, add, g);
+  // kind = qm * 2 + (layernorm ? 1 : 0)
+  static Kring fwd_ring(int kind, int nv) {
+    switch (kind) {
+      case 0: return fwd_ring_for<Q_NONE, false>(nv);
+      case 1: return fwd_ring_for<Q_NONE, true>(nv);
+      case 2: return fwd_ring_for<Q_DELAYED, false>(nv);
+      case 3: return fwd_ring_for<Q_DELAYED, true>(nv);
+      case 4: return fwd_ring_for<Q_MXFP8, false>(nv);
+      case 5: return fwd_ring_for<Q_MXFP8, true>(nv);
+      default: return nullptr;
+    }
+  }
+  template <bool LN, bool ADD>
+  static Kbring bwd_ring_for(int nv) {
+    switch (nv) {
+      case 1: return bwd_ring_kernel<Tin, LN, ADD, 1>;
+      case 2: return bwd_ring_kernel<Tin, LN, ADD, 2>;
+      case 3: return bwd_ring_kernel<Tin, LN, ADD, 3>;
+      case 4: return bwd_ring_kernel<Tin, LN, ADD, 4>;
+      case 6: return bwd_ring_kernel<Tin, LN, ADD, 6>;
+      case 8: return bwd_ring_kernel<Tin, LN, ADD, 8>;
+      default: return nullptr;
+    }
+  }
+  static Kbring bwd_ring(bool ln, bool add, int nv) {
+    if (ln) return add ? bwd_ring_for<true, true>(nv) : bwd_ring_for<true, false>(nv);
+    return add ? bwd_ring_for<false, true>(nv) : bwd_ring_for<false, false>(nv);
+  }
+  template <typename K>
+  static cudaError_t occ_smem(K k, int threads, int smem, int* occ) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, k, threads, smem);
+  }
+  static cudaError_t fwd_ring_occupancy(int qm, const RowGeom& g, int smem, int* occ) {
+    Kring k = fwd_ring(qm, g.nv);
+    return k ? occ_smem(k, g.threads, smem, occ) : cudaErrorInvalidValue;
+  }
+  static cudaError_t fwd_ring_launch(int qm, const RowGeom& g, int stages, int smem,
+                                     const FwdParams& p, int grid, cudaStream_t st) {
+    Kring k = fwd_ring(qm, g.nv);
     if (!k) return cudaErrorInvalidValue;
-    k<<<grid, g.vec == 1 ? 256 : g.threads, 0, st>>>(p);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    k<<<grid, g.threads, smem, st>>>(p, stages);
     return cudaGetLastError();
   }
+  static cudaError_t bwd_ring_occupancy(bool ln, bool add, const RowGeom& g, int smem, int* occ) {
+    Kbring k = bwd_ring(ln, add, g.nv);
+    return k ? occ_smem(k, g.threads, smem, occ) : cudaErrorInvalidValue;
+  }
+  static cudaError_t bwd_ring_launch(bool ln, bool add, const RowGeom& g, int stages, int smem,
+                                     const BwdParams& p, int grid, cudaStream_t st) {
+    Kbring k = bwd_ring(ln, add, g.nv);
+    if (!k) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    k<<<grid, g.threads, smem, st>>>(p, stages);
+    return cudaGetLastError();
+  }
+  static cudaError_t read_device_error(unsigned int* v, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(v, g_gbn_device_error, sizeof(unsigned int));
+    if (e != cudaSuccess || !clear) return e;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_gbn_device_error, &zero, sizeof(unsigned int));
+  }
+
 };
 
 }  // namespace gbn

@@ -27,7 +27,8 @@ GBN_F32, GBN_BF16, GBN_F16, GBN_E4M3, GBN_E8M0 = 0, 1, 2, 3, 4
 TORCH_DTYPE = {torch.float32: GBN_F32, torch.bfloat16: GBN_BF16, torch.float16: GBN_F16}
 
 FUNCTIONS = ("gbn_norm_fwd_workspace_size", "gbn_norm_fwd", "gbn_norm_bwd_workspace_size",
-             "gbn_norm_bwd", "gbn_status_string")
+             "gbn_norm_bwd", "gbn_device_error", "gbn_status_string")
+GBN_DEVICE_ERR_COPY_TIMEOUT = 1
 
 
 class GbnError(RuntimeError):
@@ -54,6 +55,8 @@ def _load():
     lib.gbn_norm_bwd_workspace_size.restype = I
     lib.gbn_norm_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, SZ, I64, I64, I, I, I, I, I, P]
     lib.gbn_norm_bwd.restype = I
+    lib.gbn_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), I]
+    lib.gbn_device_error.restype = I
     lib.gbn_status_string.argtypes = [I]
     lib.gbn_status_string.restype = ctypes.c_char_p
     return lib
@@ -85,6 +88,13 @@ def _stream(stream):
 
 def gbn_status_string(status: int) -> str:
     return _lib.gbn_status_string(int(status)).decode()
+
+
+def gbn_device_error(clear=True):
+    """Returns (status, flags): the sticky device-side error bits."""
+    v = ctypes.c_uint(0)
+    st = _lib.gbn_device_error(ctypes.byref(v), int(bool(clear)))
+    return st, v.value
 
 
 def gbn_norm_fwd_workspace_size(rows, hidden, in_dtype, w_dtype, out_dtype, norm_type,

@@ -216,9 +216,13 @@ def test_e4m3_hardware_conversion_matches_oracle_bit_exact(gpu, layout):
                        layout=layout, scale=scale.cuda(), amax=scale.cuda())
     torch.cuda.synchronize()
     assert torch.all(out["rsigma"] == 1.0)
-    z = (x * gamma).double().numpy()        # exact: +-gamma
+    z, _, rs = oracle.norm_fwd(x, gamma, None, 1, False, 0.0)   # exactly +-gamma (and +0)
+    assert np.all(rs == 1.0)
     q, amax, _ = oracle.quant_delayed(z, 1.0)
-    assert np.array_equal(out["out"].cpu().numpy(), q)
+    got = out["out"].cpu().numpy()
+    bad = np.argwhere(got != q)
+    detail = [(float(z[i, j]), hex(got[i, j]), hex(q[i, j])) for i, j in bad[:12]]
+    assert bad.size == 0, f"{len(bad)} codes differ: (value, gpu, oracle) {detail}"
     if layout == "rowwise_colwise":
         assert np.array_equal(out["colwise_out"].T.cpu().numpy(), q)
     assert out["updated_amax"].item() == amax
@@ -238,7 +242,7 @@ def test_e8m0_block_scales_bit_exact_on_crafted_blocks(gpu):
     out = gpu.norm_fwd(x.cuda(), gamma.cuda(), None, norm="rmsnorm", eps=0.0, scaling="mxfp8",
                        layout="rowwise_colwise")
     torch.cuda.synchronize()
-    z = (x * gamma).double().numpy()
+    z, _, _ = oracle.norm_fwd(x, gamma, None, 1, False, 0.0)
     q, s = oracle.mxfp8_rowwise(z)
     assert np.array_equal(out["scale_inv"].cpu().numpy(), s)
     assert np.array_equal(out["out"].cpu().numpy(), q)
