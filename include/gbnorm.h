@@ -175,6 +175,33 @@ gbn_status gbn_norm_bwd(const void* dz, const void* x, const float* mu, const fl
                         gbn_norm_type norm_type, int zero_centered_gamma, int sm_margin,
                         cudaStream_t stream);
 
+/* Backward without a caller-provided workspace.  The pages have no
+ * counterpart: this entry point exists for callers that cannot allocate
+ * device memory at the call site -- code running inside a region whose
+ * device-memory plan is fixed (for example while a framework records a
+ * replayable graph of its launches), behind a custom allocator that must not
+ * be re-entered from here, or in plugin hosts that forbid device allocation.
+ * gbn_norm_bwd needs a workspace for its per-CTA partials; this variant uses
+ * a fixed 32 MiB scratch array that lives in the library's device image
+ * (every GPU that loads the library holds it until the process exits) and
+ * otherwise behaves exactly like gbn_norm_bwd (same arguments, minus the
+ * workspace).
+ *   - It allocates nothing: no cudaMalloc/cudaFree or allocating library call.
+ *   - The first call on a device looks up the scratch array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - All calls share the one scratch array (it keeps the last call's
+ *     contents; the backward overwrites every partial it reads), so calls
+ *     that overlap on the GPU -- on different streams, or from several host
+ *     threads -- race.  Serialize them.
+ *   - Returns GBN_ERR_WORKSPACE when the problem's partials
+ *     (gbn_norm_bwd_workspace_size) exceed 32 MiB. */
+gbn_status gbn_norm_bwd_noalloc(const void* dz, const void* x, const float* mu,
+                                const float* rsigma, const void* gamma, const void* dresidual,
+                                void* dx, void* dgamma, void* dbeta, int64_t rows,
+                                int64_t hidden, gbn_dtype in_dtype, gbn_dtype w_dtype,
+                                gbn_norm_type norm_type, int zero_centered_gamma, int sm_margin,
+                                cudaStream_t stream);
+
 /* Device-side error bits, sticky across calls on the current device:
  *   bit 0 (GBN_DEVICE_ERR_COPY_TIMEOUT): a kernel waited longer than 2 s for
  *   one of its own bulk copies into shared memory, stopped early and left

@@ -27,7 +27,7 @@ GBN_F32, GBN_BF16, GBN_F16, GBN_E4M3, GBN_E8M0 = 0, 1, 2, 3, 4
 TORCH_DTYPE = {torch.float32: GBN_F32, torch.bfloat16: GBN_BF16, torch.float16: GBN_F16}
 
 FUNCTIONS = ("gbn_norm_fwd_workspace_size", "gbn_norm_fwd", "gbn_norm_bwd_workspace_size",
-             "gbn_norm_bwd", "gbn_device_error", "gbn_status_string")
+             "gbn_norm_bwd", "gbn_norm_bwd_noalloc", "gbn_device_error", "gbn_status_string")
 GBN_DEVICE_ERR_COPY_TIMEOUT = 1
 
 
@@ -55,6 +55,8 @@ def _load():
     lib.gbn_norm_bwd_workspace_size.restype = I
     lib.gbn_norm_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, SZ, I64, I64, I, I, I, I, I, P]
     lib.gbn_norm_bwd.restype = I
+    lib.gbn_norm_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I64, I64, I, I, I, I, I, P]
+    lib.gbn_norm_bwd_noalloc.restype = I
     lib.gbn_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), I]
     lib.gbn_device_error.restype = I
     lib.gbn_status_string.argtypes = [I]
@@ -140,3 +142,13 @@ def gbn_norm_bwd(dz, x, mu, rsigma, gamma, dresidual, dx, dgamma, dbeta, workspa
                              _ptr(workspace), workspace_bytes, rows, hidden, in_dtype, w_dtype,
                              norm_type, int(bool(zero_centered_gamma)), sm_margin,
                              _stream(stream))
+
+
+def gbn_norm_bwd_noalloc(dz, x, mu, rsigma, gamma, dresidual, dx, dgamma, dbeta, rows, hidden,
+                         in_dtype, w_dtype, norm_type, zero_centered_gamma, sm_margin,
+                         stream=None) -> int:
+    """The backward on the library's fixed scratch array (no workspace)."""
+    return _lib.gbn_norm_bwd_noalloc(_ptr(dz), _ptr(x), _ptr(mu), _ptr(rsigma), _ptr(gamma),
+                                     _ptr(dresidual), _ptr(dx), _ptr(dgamma), _ptr(dbeta), rows,
+                                     hidden, in_dtype, w_dtype, norm_type,
+                                     int(bool(zero_centered_gamma)), sm_margin, _stream(stream))
