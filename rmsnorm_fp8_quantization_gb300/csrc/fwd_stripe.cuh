@@ -236,16 +236,20 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
       }
       const int col = c0 + 4 * cg;
       const Tin* xcol = xs + 4 * cg;
-      // z of row r as two pairs
-      auto zrow = [&](int r, uint64_t& z01, uint64_t& z23) {
+      // z of row r as two pairs, with weights (ga, gb) and betas (ba, bb)
+      auto zrow_w = [&](int r, uint64_t ga, uint64_t gb, uint64_t ba, uint64_t bb, uint64_t& z01,
+                        uint64_t& z23) {
         const float2 st = rstat[r];
         const uint64_t m2 = p2(st.x, st.x), r2 = p2(st.y, st.y);
         uint64_t xp[2];
         lds4_pairs<Tin>(xcol + r * hc, xp);
         const uint64_t t01 = mul2(LN ? sub2(xp[0], m2) : xp[0], r2);
         const uint64_t t23 = mul2(LN ? sub2(xp[1], m2) : xp[1], r2);
-        z01 = LN ? fma2(t01, g01, b01) : mul2(t01, g01);
-        z23 = LN ? fma2(t23, g23, b23) : mul2(t23, g23);
+        z01 = LN ? fma2(t01, ga, ba) : mul2(t01, ga);
+        z23 = LN ? fma2(t23, gb, bb) : mul2(t23, gb);
+      };
+      auto zrow = [&](int r, uint64_t& z01, uint64_t& z23) {
+        zrow_w(r, g01, g23, b01, b23, z01, z23);
       };
       auto absmax4 = [](uint64_t a, uint64_t b) {
         const float2 x = u2(a), y = u2(b);
@@ -279,6 +283,9 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
       } else {
         // pass 1: rowwise MXFP8 (a 1x32 block is 8 lanes) and the column amax
         float cm[4] = {0.f, 0.f, 0.f, 0.f};
+        uint8_t* sc = p.write_rowwise ? p.mx_scale + i0 * (H / 32) + col / 32 : nullptr;
+        const int64_t sc_stride = H / 32;
+#pragma unroll 4
         for (int r = 0; r < kStripeRows; ++r) {
           uint64_t z01, z23;
           zrow(r, z01, z23);
@@ -295,13 +302,13 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
             for (int o = 1; o < 8; o <<= 1) a = fmax_nan(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
             const uint32_t code = e8m0_code(a);
             const float m = e8m0_mult(code);
-            *reinterpret_cast<uint32_t*>(orow + static_cast<int64_t>(r) * H) =
-                e4m3x4_pairs(z01, z23, p2(m, m));
-            if ((cg & 7) == 0)
-              p.mx_scale[(i0 + r) * (H / 32) + col / 32] = static_cast<uint8_t>(code);
+            *reinterpret_cast<uint32_t*>(orow) = e4m3x4_pairs(z01, z23, p2(m, m));
+            if ((cg & 7) == 0) *sc = static_cast<uint8_t>(code);
+            orow += H;
+            sc += sc_stride;
           }
         }
-        // pass 2: 32x1 column blocks
+        // pass 2: 32x1 column blocks; the block multiplier is folded into g'
         if (p.write_colwise) {
           uint32_t codes = 0;
           float mul[4];
@@ -312,14 +319,20 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
             codes |= code << (8 * c);
           }
           *reinterpret_cast<uint32_t*>(p.mx_colwise_scale + stripe_of(k) * H + col) = codes;
+          // A power-of-two multiplier commutes exactly with the roundings of
+          // (x - mu) * rs * g' + beta (while g' and beta times it stay normal),
+          // so it is applied to g' and beta once.
           const uint64_t m01 = p2(mul[0], mul[1]), m23 = p2(mul[2], mul[3]);
+          const uint64_t gm01 = mul2(g01, m01), gm23 = mul2(g23, m23);
+          const uint64_t bm01 = mul2(b01, m01), bm23 = mul2(b23, m23);
           uint8_t* crow = p.colwise_out + i0 * H + col;
+#pragma unroll 4
           for (int r = 0; r < kStripeRows; ++r) {
             uint64_t z01, z23;
-            zrow(r, z01, z23);
-            const float2 x = u2(mul2(z01, m01)), y = u2(mul2(z23, m23));
-            *reinterpret_cast<uint32_t*>(crow + static_cast<int64_t>(r) * H) =
-                e4m3x2(x.x, x.y) | (e4m3x2(y.x, y.y) << 16);
+            zrow_w(r, gm01, gm23, bm01, bm23, z01, z23);
+            const float2 x = u2(z01), y = u2(z23);
+            *reinterpret_cast<uint32_t*>(crow) = e4m3x2(x.x, x.y) | (e4m3x2(y.x, y.y) << 16);
+            crow += H;
           }
         }
       }

@@ -307,11 +307,19 @@ __global__ void __launch_bounds__(bwd_max_threads(NV)) bwd_ring_kernel(const Bwd
   int st = 0;          // stage of row k
   uint32_t phase = 0;  // its mbarrier phase parity
   int64_t k = 0;
+  // Row statistics are loaded one row ahead so their latency is hidden.
+  float mu_next = 0.f, rs_next = 0.f;
+  if (sched.count > 0) {
+    if constexpr (LN) mu_next = p.mu[sched.row(0)];
+    rs_next = p.rsigma[sched.row(0)];
+  }
   for (; k < sched.count; ++k, st = st + 1 == stages ? 0 : st + 1, phase ^= (st == 0)) {
     const int64_t row = sched.row(k);
-    // Row statistics first: their latency overlaps the wait for the stage.
-    const float mu = LN ? p.mu[row] : 0.f;
-    const float rs = p.rsigma[row];
+    const float mu = mu_next, rs = rs_next;
+    if (k + 1 < sched.count) {
+      if constexpr (LN) mu_next = p.mu[row + sched.stride];
+      rs_next = p.rsigma[row + sched.stride];
+    }
     if (!mbar_wait(&full[st], phase)) s_abort = 1;
     const uint8_t* sb = ring + st * stage_bytes;
     uint32_t dzw[NV][NW], xw[NV][NW], rw[ADD ? NV : 1][NW];
