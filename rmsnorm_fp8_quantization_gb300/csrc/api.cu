@@ -62,9 +62,9 @@ int bwd_threads_cap(int nv) { return bwd_max_threads(nv); }
 // 8 and of the 16-byte vector; of 128 for MXFP8), at most 2048 two-byte or
 // 1024 four-byte columns, with the slice (or two, when they fit) in shared
 // memory.  Among them the one with the most co-resident CTAs (clusters x C;
-// packing differs per C, and small slices fit two CTAs per SM) wins; ties go
-// to two stages, then to the smaller cluster.  Cached per (device, dtype,
-// mode, hidden).
+// packing differs per C, and small slices fit several CTAs per SM), weighted
+// by the share of threads that have work, wins; ties go to two stages, then to
+// the smaller cluster.  Cached per (device, dtype, mode, hidden).
 bool stripe_geom(const KernelTable& kt, int in, int qm, bool ln, int64_t hidden, int esize,
                  int sms, StripeGeom* out) {
   static std::mutex mu;
@@ -96,7 +96,12 @@ bool stripe_geom(const KernelTable& kt, int in, int qm, bool ln, int64_t hidden,
       StripeGeom g{c, static_cast<int>(hc), stages, smem, 0};
       int n = 0;
       if (kt.stripe_max_clusters(qm, ln, g, &n) != cudaSuccess || n < 1) continue;
-      const int active = n * c;  // co-resident CTAs
+      // co-resident CTAs, weighted by the share of each CTA's threads that
+      // get a 4-column item (hc/4 items over kStripeThreads threads)
+      const int64_t items = hc / 4;
+      const int64_t waves = (items + kStripeThreads - 1) / kStripeThreads;
+      const int active = static_cast<int>(static_cast<int64_t>(n) * c * 1024 * items /
+                                          (waves * kStripeThreads) / 1024);
       if (active > best_active) {  // strict: earlier (2 stages, smaller C) wins ties
         best_active = active;
         best = g;

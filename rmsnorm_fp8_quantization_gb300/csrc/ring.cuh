@@ -118,12 +118,12 @@ __global__ void __launch_bounds__(fwd_ring_max_threads(NV)) fwd_ring_kernel(cons
     uint64_t acc0 = 0ull, acc1 = 0ull;  // two chains of pairs
 #pragma unroll
     for (int kk = 0; kk < NV; ++kk) {
+      // Branch-free: a thread past the row's end reads the last vector and
+      // zeroes it.
       const int v = kk * T + tid;
-      uint32_t w[NW] = {0u, 0u, 0u, 0u};
-      if (v < nvec) {
-        const uint4 r = *reinterpret_cast<const uint4*>(xs + v * VEC);
-        w[0] = r.x; w[1] = r.y; w[2] = r.z; w[3] = r.w;
-      }
+      const bool act = v < nvec;
+      const uint4 r = *reinterpret_cast<const uint4*>(xs + (act ? v : nvec - 1) * VEC);
+      const uint32_t w[NW] = {act ? r.x : 0u, act ? r.y : 0u, act ? r.z : 0u, act ? r.w : 0u};
       widen_pairs<Tin, VEC>(w, xp[kk]);
 #pragma unroll
       for (int i = 0; i < NP; ++i) {
@@ -325,23 +325,20 @@ __global__ void __launch_bounds__(bwd_max_threads(NV)) bwd_ring_kernel(const Bwd
     uint32_t dzw[NV][NW], xw[NV][NW], rw[ADD ? NV : 1][NW];
 #pragma unroll
     for (int kk = 0; kk < NV; ++kk) {
+      // Branch-free: a thread past the row's end reads the last vector and
+      // zeroes it (zero dz and x contribute nothing to any sum).
       const int v = kk * T + tid;
-      if (v < nvec) {
-        const uint4 a = *reinterpret_cast<const uint4*>(sb + v * 16);
-        const uint4 b = *reinterpret_cast<const uint4*>(sb + slot + v * 16);
-        dzw[kk][0] = a.x; dzw[kk][1] = a.y; dzw[kk][2] = a.z; dzw[kk][3] = a.w;
-        xw[kk][0] = b.x; xw[kk][1] = b.y; xw[kk][2] = b.z; xw[kk][3] = b.w;
-        if constexpr (ADD) {
-          const uint4 c = *reinterpret_cast<const uint4*>(sb + 2 * slot + v * 16);
-          rw[kk][0] = c.x; rw[kk][1] = c.y; rw[kk][2] = c.z; rw[kk][3] = c.w;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < NW; ++i) {
-          dzw[kk][i] = 0u;
-          xw[kk][i] = 0u;
-          if constexpr (ADD) rw[kk][i] = 0u;
-        }
+      const bool act = v < nvec;
+      const int vl = act ? v : nvec - 1;
+      const uint4 a = *reinterpret_cast<const uint4*>(sb + vl * 16);
+      const uint4 b = *reinterpret_cast<const uint4*>(sb + slot + vl * 16);
+      dzw[kk][0] = act ? a.x : 0u; dzw[kk][1] = act ? a.y : 0u;
+      dzw[kk][2] = act ? a.z : 0u; dzw[kk][3] = act ? a.w : 0u;
+      xw[kk][0] = act ? b.x : 0u; xw[kk][1] = act ? b.y : 0u;
+      xw[kk][2] = act ? b.z : 0u; xw[kk][3] = act ? b.w : 0u;
+      if constexpr (ADD) {
+        const uint4 c = *reinterpret_cast<const uint4*>(sb + 2 * slot + vl * 16);
+        rw[kk][0] = c.x; rw[kk][1] = c.y; rw[kk][2] = c.z; rw[kk][3] = c.w;
       }
     }
     const uint64_t mu2 = p2(mu, mu), rs2 = p2(rs, rs);
