@@ -88,7 +88,7 @@ bool stripe_geom(const KernelTable& kt, int in, int qm, bool ln, int64_t hidden,
   for (int c = 1; c <= 8; ++c) {
     if (hidden % c) continue;
     const int64_t hc = hidden / c;
-    // 16-byte vectors; MXFP8 row blocks of 32 = 8 lanes of 4 columns, in whole warps.
+    // 16-byte vectors; MXFP8 in whole bands of 16 vectors (hc % 128 for 2- and 4-byte inputs).
     if (hc % vec || hc % 8 || (qm == Q_MXFP8 && hc % 128) || hc > hc_max) continue;
     for (int stages = 2; stages >= 1; --stages) {
       const int smem = stripe_smem_bytes(qm, ln, static_cast<int>(hc), esize, stages);
@@ -97,11 +97,13 @@ bool stripe_geom(const KernelTable& kt, int in, int qm, bool ln, int64_t hidden,
       int n = 0;
       if (kt.stripe_max_clusters(qm, ln, g, &n) != cudaSuccess || n < 1) continue;
       // co-resident CTAs, weighted by the share of each CTA's threads that
-      // get a 4-column item (hc/4 items over kStripeThreads threads)
-      const int64_t items = hc / 4;
-      const int64_t waves = (items + kStripeThreads - 1) / kStripeThreads;
-      const int active = static_cast<int>(static_cast<int64_t>(n) * c * 1024 * items /
-                                          (waves * kStripeThreads) / 1024);
+      // have work: delayed scaling gives a thread a 4-column item (hc/4 items
+      // over kStripeThreads threads), MXFP8 a warp a band of 16 vectors.
+      const int64_t workers = qm == Q_MXFP8 ? hc / vec / 16 : hc / 4;
+      const int64_t slots = qm == Q_MXFP8 ? kStripeThreads / 32 : kStripeThreads;
+      const int64_t waves = (workers + slots - 1) / slots;
+      const int active = static_cast<int>(static_cast<int64_t>(n) * c * 1024 * workers /
+                                          (waves * slots) / 1024);
       if (active > best_active) {  // strict: earlier (2 stages, smaller C) wins ties
         best_active = active;
         best = g;
@@ -156,7 +158,7 @@ RingChoice choose_ring(int key_kind, int in, const RowGeom& g, int stage_bytes, 
   }
   // Bytes in flight per SM up to kRingTarget count first, then resident
   // threads (latency hiding), then fewer stages.
-  constexpr int64_t kRingTarget = 128 * 1024;
+  constexpr int64_t kRingTarget = 224 * 1024;
   RingChoice best;
   int64_t best_inflight = -1;
   int best_occ = 0;
@@ -348,7 +350,7 @@ gbn_status gbn_norm_fwd(const void* x, const void* gamma, const void* beta, cons
   if (colwise) {
     StripeGeom sg;
     const bool stripe_ok = vec_ok && rows % 32 == 0 && aligned(colwise_out, 32) &&
-                           (qm != Q_MXFP8 || aligned(colwise_scale_inv, 4)) &&
+                           (qm != Q_MXFP8 || aligned(colwise_scale_inv, vec >= 8 ? 8 : 4)) &&
                            stripe_geom(kt, in_dtype, qm, ln, hidden, esize(in_dtype), sms, &sg);
     if (stripe_ok) {
       int64_t ncl = static_cast<int64_t>(static_cast<double>(sg.max_clusters) * esms / sms);
@@ -363,7 +365,7 @@ gbn_status gbn_norm_fwd(const void* x, const void* gamma, const void* beta, cons
   RowGeom gr;
   if (vec_ok && row_geom(hidden / vec, vec, 4, fwd_ring_cap, &gr)) {
     // Rows streamed through a shared-memory ring by bulk copies.
-    const int stage_bytes = static_cast<int>((hidden * esize(in_dtype) + 127) / 128 * 128);
+    const int stage_bytes = ring_slot_bytes(gr.nv, gr.threads);
     const int kind = qm * 2 + (ln ? 1 : 0);
     const RingChoice rc = choose_ring(10 + kind, in_dtype, gr, stage_bytes, kMaxRingStagesHost,
                                       [&](int smem, int* o) {

@@ -19,11 +19,13 @@
 //      CTA merges the C partials of a row in rank order (identical results in
 //      all CTAs); no cluster-wide barrier per stripe.
 //   3. A thread item is 4 adjacent columns x all 32 rows, computed in packed
-//      fp32 pairs: rowwise codes go to HBM as 4-byte words (a warp writes 128
-//      contiguous bytes of a row); delayed codes are transposed in registers
-//      (4x4 byte transposes) and each column's 32 codes leave as one 32-byte
-//      store, a whole sector; MXFP8 row blocks reduce their amax over 8
-//      lanes, and each 32x1 column block lies inside one thread.
+//      fp32 pairs.  Delayed scaling: rowwise codes go to HBM as 4-byte words
+//      (a warp writes 128 contiguous bytes of a row); the codes are transposed
+//      in registers (4x4 byte transposes) and each column's 32 codes leave as
+//      one 32-byte store, a whole sector.  MXFP8: each 32x1 column block lies
+//      inside one thread (a pass for the column amax, a pass for the codes);
+//      the rowwise 1x32 blocks are done before, by warps walking rows in
+//      16-byte vectors (a block is 32/VEC adjacent lanes).
 // x is read from HBM once.
 #pragma once
 
@@ -224,7 +226,120 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
     }
     __syncthreads();
 
-    // ---- 3. items of 4 columns x 32 rows
+    // ---- 3, MXFP8: a warp owns a band of 16 vectors (16*VEC columns) over the
+    // 32 rows; lane = (vector vl, row parity rp) walks rows rp, rp+2, ...
+    // A 1x32 row block is 32/VEC adjacent lanes (shuffles); a 32x1 column
+    // block is one lane's 16 rows plus its partner lane^16's.  Pass 1 writes
+    // the rowwise codes and keeps the column amax; pass 2 the colwise codes.
+    if constexpr (QM == Q_MXFP8) {
+      constexpr int NPV = VEC / 2;
+      constexpr int TPB = 32 / VEC;
+      const int vl = lane & 15, rp = lane >> 4;
+      const int nbands = nvs / 16;
+      const int64_t sc_stride = H / 32;
+      for (int band = warp; band < nbands; band += kStripeWarps) {
+        const int v = band * 16 + vl;
+        const int col = c0 + v * VEC;
+        uint64_t gw[NPV], bw[NPV];
+#pragma unroll
+        for (int h = 0; h < NPV / 2; ++h) {
+          const float4 g = reinterpret_cast<const float4*>(wg + v * VEC)[h];
+          gw[2 * h] = p2(g.x, g.y);
+          gw[2 * h + 1] = p2(g.z, g.w);
+          if constexpr (LN) {
+            const float4 bv = reinterpret_cast<const float4*>(wb + v * VEC)[h];
+            bw[2 * h] = p2(bv.x, bv.y);
+            bw[2 * h + 1] = p2(bv.z, bv.w);
+          } else {
+            bw[2 * h] = bw[2 * h + 1] = 0ull;
+          }
+        }
+        const uint4* xv = reinterpret_cast<const uint4*>(xs + rp * hc) + v;
+        const int xstep = 2 * nvs;  // vectors between rows r and r + 2
+        // z of the lane's vector in row r, as NPV pairs, with weights g, b
+        auto zvec = [&](int r, const uint64_t* g, const uint64_t* bb, uint64_t* z) {
+          const float2 st = rstat[r];
+          const uint64_t m2 = p2(st.x, st.x), r2 = p2(st.y, st.y);
+          const uint4 u = xv[(r >> 1) * xstep];
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+          widen_pairs<Tin, VEC>(w, z);
+#pragma unroll
+          for (int i = 0; i < NPV; ++i) {
+            const uint64_t t = mul2(LN ? sub2(z[i], m2) : z[i], r2);
+            z[i] = LN ? fma2(t, g[i], bb[i]) : mul2(t, g[i]);
+          }
+        };
+        float cm[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) cm[e] = 0.f;
+        uint8_t* orow = p.write_rowwise ? reinterpret_cast<uint8_t*>(p.out) + (i0 + rp) * H + col
+                                        : nullptr;
+        uint8_t* srow = p.write_rowwise ? p.mx_scale + (i0 + rp) * sc_stride + col / 32 : nullptr;
+#pragma unroll 2
+        for (int r = rp; r < kStripeRows; r += 2) {
+          uint64_t z[NPV];
+          zvec(r, gw, bw, z);
+          float a = 0.f;
+#pragma unroll
+          for (int i = 0; i < NPV; ++i) {
+            const float2 f = u2(z[i]);
+            cm[2 * i] = fmax_nan(cm[2 * i], fabsf(f.x));
+            cm[2 * i + 1] = fmax_nan(cm[2 * i + 1], fabsf(f.y));
+            a = fmax_nan(a, fmax_nan(fabsf(f.x), fabsf(f.y)));
+          }
+          if (p.write_rowwise) {
+#pragma unroll
+            for (int o = 1; o < TPB; o <<= 1) a = fmax_nan(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+            const uint32_t code = e8m0_code(a);
+            const float m = e8m0_mult(code);
+            const uint64_t s2 = p2(m, m);
+            uint32_t q[VEC / 4];
+#pragma unroll
+            for (int i = 0; i < VEC / 4; ++i) q[i] = e4m3x4_pairs(z[2 * i], z[2 * i + 1], s2);
+            st_words<VEC / 4>(orow, q);
+            if ((v & (TPB - 1)) == 0) *srow = static_cast<uint8_t>(code);
+            orow += 2 * H;
+            srow += 2 * sc_stride;
+          }
+        }
+        if (p.write_colwise) {
+          uint32_t cw[VEC / 4];
+          uint64_t gm[NPV], bm[NPV];
+#pragma unroll
+          for (int i = 0; i < NPV; ++i) {
+            const float c0a = fmax_nan(cm[2 * i], __shfl_xor_sync(0xFFFFFFFFu, cm[2 * i], 16));
+            const float c1a = fmax_nan(cm[2 * i + 1], __shfl_xor_sync(0xFFFFFFFFu, cm[2 * i + 1], 16));
+            const uint32_t k0 = e8m0_code(c0a), k1 = e8m0_code(c1a);
+            if ((i & 1) == 0) cw[i / 2] = 0u;
+            cw[i / 2] |= (k0 | (k1 << 8)) << (16 * (i & 1));
+            // A power-of-two multiplier commutes exactly with the roundings
+            // of (x - mu) * rs * g' + beta (while g' and beta times it stay
+            // normal), so it is applied to g' and beta once.
+            const uint64_t m01 = p2(e8m0_mult(k0), e8m0_mult(k1));
+            gm[i] = mul2(gw[i], m01);
+            bm[i] = mul2(bw[i], m01);
+          }
+          if (rp == 0) st_words<VEC / 4>(p.mx_colwise_scale + stripe_of(k) * H + col, cw);
+          uint8_t* crow = p.colwise_out + (i0 + rp) * H + col;
+#pragma unroll 2
+          for (int r = rp; r < kStripeRows; r += 2) {
+            uint64_t z[NPV];
+            zvec(r, gm, bm, z);
+            uint32_t q[VEC / 4];
+#pragma unroll
+            for (int i = 0; i < VEC / 4; ++i) {
+              const float2 fa = u2(z[2 * i]), fb = u2(z[2 * i + 1]);
+              q[i] = e4m3x2(fa.x, fa.y) | (e4m3x2(fb.x, fb.y) << 16);
+            }
+            st_words<VEC / 4>(crow, q);
+            crow += 2 * H;
+          }
+        }
+      }
+    }
+
+    // ---- 3, delayed scaling: items of 4 columns x 32 rows
+    if constexpr (QM == Q_DELAYED)
     for (int cg = tid; cg < G; cg += kStripeThreads) {
       const float4 g4 = reinterpret_cast<const float4*>(wg)[cg];
       const uint64_t g01 = p2(g4.x, g4.y), g23 = p2(g4.z, g4.w);
@@ -255,8 +370,8 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
         const float2 x = u2(a), y = u2(b);
         return fmax_nan(fmax_nan(fabsf(x.x), fabsf(x.y)), fmax_nan(fabsf(y.x), fabsf(y.y)));
       };
-      uint8_t* orow = p.write_rowwise ? reinterpret_cast<uint8_t*>(p.out) + i0 * H + col : nullptr;
       if constexpr (QM == Q_DELAYED) {
+        uint8_t* orow = p.write_rowwise ? reinterpret_cast<uint8_t*>(p.out) + i0 * H + col : nullptr;
         const uint64_t s2 = p2(qscale, qscale);
         uint32_t w[kStripeRows];
 #pragma unroll
@@ -279,61 +394,6 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
 #pragma unroll
           for (int c = 0; c < 4; ++c)
             st_global_v8(p.colwise_out + static_cast<int64_t>(col + c) * N + i0, o[c]);
-        }
-      } else {
-        // pass 1: rowwise MXFP8 (a 1x32 block is 8 lanes) and the column amax
-        float cm[4] = {0.f, 0.f, 0.f, 0.f};
-        uint8_t* sc = p.write_rowwise ? p.mx_scale + i0 * (H / 32) + col / 32 : nullptr;
-        const int64_t sc_stride = H / 32;
-#pragma unroll 4
-        for (int r = 0; r < kStripeRows; ++r) {
-          uint64_t z01, z23;
-          zrow(r, z01, z23);
-          {
-            const float2 x = u2(z01), y = u2(z23);
-            cm[0] = fmax_nan(cm[0], fabsf(x.x));
-            cm[1] = fmax_nan(cm[1], fabsf(x.y));
-            cm[2] = fmax_nan(cm[2], fabsf(y.x));
-            cm[3] = fmax_nan(cm[3], fabsf(y.y));
-          }
-          if (p.write_rowwise) {
-            float a = absmax4(z01, z23);
-#pragma unroll
-            for (int o = 1; o < 8; o <<= 1) a = fmax_nan(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
-            const uint32_t code = e8m0_code(a);
-            const float m = e8m0_mult(code);
-            *reinterpret_cast<uint32_t*>(orow) = e4m3x4_pairs(z01, z23, p2(m, m));
-            if ((cg & 7) == 0) *sc = static_cast<uint8_t>(code);
-            orow += H;
-            sc += sc_stride;
-          }
-        }
-        // pass 2: 32x1 column blocks; the block multiplier is folded into g'
-        if (p.write_colwise) {
-          uint32_t codes = 0;
-          float mul[4];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint32_t code = e8m0_code(cm[c]);
-            mul[c] = e8m0_mult(code);
-            codes |= code << (8 * c);
-          }
-          *reinterpret_cast<uint32_t*>(p.mx_colwise_scale + stripe_of(k) * H + col) = codes;
-          // A power-of-two multiplier commutes exactly with the roundings of
-          // (x - mu) * rs * g' + beta (while g' and beta times it stay normal),
-          // so it is applied to g' and beta once.
-          const uint64_t m01 = p2(mul[0], mul[1]), m23 = p2(mul[2], mul[3]);
-          const uint64_t gm01 = mul2(g01, m01), gm23 = mul2(g23, m23);
-          const uint64_t bm01 = mul2(b01, m01), bm23 = mul2(b23, m23);
-          uint8_t* crow = p.colwise_out + i0 * H + col;
-#pragma unroll 4
-          for (int r = 0; r < kStripeRows; ++r) {
-            uint64_t z01, z23;
-            zrow_w(r, gm01, gm23, bm01, bm23, z01, z23);
-            const float2 x = u2(z01), y = u2(z23);
-            *reinterpret_cast<uint32_t*>(crow) = e4m3x2(x.x, x.y) | (e4m3x2(y.x, y.y) << 16);
-            crow += H;
-          }
         }
       }
     }

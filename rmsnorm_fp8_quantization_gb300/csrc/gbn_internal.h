@@ -90,6 +90,11 @@ constexpr int fwd_ring_max_threads(int nv) {
   return nv <= 1 ? 1024 : nv == 2 ? 768 : nv == 3 ? 640 : nv == 4 ? 512 : nv == 6 ? 384 : 256;
 }
 
+// Bytes of one stage of the forward ring: the NV * threads vectors a CTA
+// covers, rounded up to 128 bytes.  The tail past the row stays zero, so the
+// row loop reads every vector without a bounds test.
+__host__ __device__ constexpr int ring_slot_bytes(int nv, int threads) { return (nv * threads * 16 + 127) / 128 * 128; }
+
 constexpr int kStripeRows = 32;
 constexpr int kStripeThreads = 256;
 

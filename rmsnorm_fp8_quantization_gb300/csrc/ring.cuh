@@ -13,6 +13,8 @@
 // (Description, I/O Contract) for the residual add.
 #pragma once
 
+#include <type_traits>
+
 #include "gbn_device.cuh"
 
 namespace gbn {
@@ -56,18 +58,50 @@ __device__ __forceinline__ void load_weight_pairs(const void* base, int wdt, int
   for (int i = 0; i < VEC / 2; ++i) out[i] = p2(f[2 * i] + add, f[2 * i + 1] + add);
 }
 
+// Zeroes bytes [from, slot) of each of the n slots (slot apart) starting at
+// base, cooperatively over the CTA.  `from` and `slot` are multiples of 16.
+__device__ __forceinline__ void zero_slot_tails(uint8_t* base, int n, uint32_t slot,
+                                                uint32_t from) {
+  for (int q = 0; q < n; ++q)
+    for (uint32_t b = from + 16u * threadIdx.x; b < slot; b += 16u * blockDim.x)
+      *reinterpret_cast<uint4*>(base + q * slot + b) = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// Block sum for the row kernels.  buf: 32 floats whose entries at and past
+// nwarps are zero.  Up to 8 warps, every thread adds the warp partials from
+// shared memory in one fixed order (no second shuffle tree).
+__device__ __forceinline__ float row_block_sum(float v, float* buf, int lane, int warp,
+                                               int nwarps) {
+  v = warp_sum(v);
+  if (nwarps == 1) return v;
+  if (lane == 0) buf[warp] = v;
+  __syncthreads();
+  if (nwarps <= 8) {
+    const float4 a = *reinterpret_cast<const float4*>(buf);
+    float r = (a.x + a.y) + (a.z + a.w);
+    if (nwarps > 4) {
+      const float4 b = *reinterpret_cast<const float4*>(buf + 4);
+      r += (b.x + b.y) + (b.z + b.w);
+    }
+    return r;
+  }
+  return warp_sum(lane < nwarps ? buf[lane] : 0.f);
+}
 // Forward row pass.  Thread t owns vectors v = k*T + t (k < NV) of every row;
 // its g' / beta stay in registers for the whole kernel as fp32 pairs, the row
 // is widened to pairs once and all arithmetic runs two lanes per instruction.
+// A stage slot holds NV*T vectors; the part past the row is zero, so the
+// loads need no bounds test (zeros add nothing to either sum).
 template <typename Tin, int QM, bool LN, int NV>
 __global__ void __launch_bounds__(fwd_ring_max_threads(NV)) fwd_ring_kernel(const FwdParams p,
                                                                            const int stages) {
   constexpr int VEC = 16 / (int)sizeof(Tin);
   constexpr int NW = Words<Tin, VEC>::n;
   constexpr int NP = VEC / 2;
+  using Tout = typename std::conditional<QM == Q_NONE, Tin, uint8_t>::type;
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ uint64_t full[kMaxRingStages];
-  __shared__ float red[2][32];
+  __shared__ __align__(16) float red[2][32];
   __shared__ int s_abort;
   const int tid = threadIdx.x, T = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5, nwarps = T >> 5;
@@ -75,25 +109,28 @@ __global__ void __launch_bounds__(fwd_ring_max_threads(NV)) fwd_ring_kernel(cons
   const int nvec = H / VEC;
   const float inv_h = 1.f / static_cast<float>(H);
   const uint32_t row_bytes = static_cast<uint32_t>(H) * sizeof(Tin);
-  const uint32_t stage_bytes = (row_bytes + 127u) & ~127u;
-  const Tin* x = reinterpret_cast<const Tin*>(p.x);
+  const uint32_t stage_bytes = static_cast<uint32_t>(ring_slot_bytes(NV, T));
   const RowSchedule sched(p.rows);
+  const int64_t row_step = sched.stride * H;  // elements between this CTA's rows
   float qscale = 1.f;
   if constexpr (QM == Q_DELAYED) qscale = *p.scale;
   const uint64_t qscale2 = p2(qscale, qscale);
   float amax_t = 0.f;
 
   int64_t issued = 0;
+  const Tin* src = reinterpret_cast<const Tin*>(p.x) + sched.first * H;  // next row to fetch
   if (tid == 0) {
     s_abort = 0;
     for (int s = 0; s < stages; ++s) mbar_init(&full[s], 1);
     fence_mbar_init();
-    for (; issued < stages && issued < sched.count; ++issued) {
+    for (; issued < stages && issued < sched.count; ++issued, src += row_step) {
       const int s = static_cast<int>(issued);
       mbar_arrive_expect_tx(&full[s], row_bytes);
-      bulk_g2s(ring + s * stage_bytes, x + sched.row(issued) * H, row_bytes, &full[s]);
+      bulk_g2s(ring + s * stage_bytes, src, row_bytes, &full[s]);
     }
   }
+  for (int i = tid; i < 64; i += T) (&red[0][0])[i] = 0.f;
+  zero_slot_tails(ring, stages, stage_bytes, row_bytes);
   uint64_t gw[NV][NP], bw[LN ? NV : 1][NP];
   {
     const float gadd = p.zcg ? 1.f : 0.f;
@@ -106,24 +143,23 @@ __global__ void __launch_bounds__(fwd_ring_max_threads(NV)) fwd_ring_kernel(cons
   }
   __syncthreads();
 
+  // This thread's first element in the current row, in the input stage and
+  // in the output.
+  const uint8_t* xs = ring + tid * 16;
+  Tout* orow = reinterpret_cast<Tout*>(p.out) + sched.first * H + tid * VEC;
+  const int64_t vstep = static_cast<int64_t>(T) * VEC;  // elements between k-vectors
   int rb = 0;
   int st = 0;          // stage of row k
   uint32_t phase = 0;  // its mbarrier phase parity
   int64_t k = 0;
-  for (; k < sched.count; ++k, st = st + 1 == stages ? 0 : st + 1, phase ^= (st == 0)) {
-    const int64_t row = sched.row(k);
+  for (; k < sched.count; ++k, orow += row_step) {
     if (!mbar_wait(&full[st], phase)) s_abort = 1;
-    const Tin* xs = reinterpret_cast<const Tin*>(ring + st * stage_bytes);
     uint64_t xp[NV][NP];
     uint64_t acc0 = 0ull, acc1 = 0ull;  // two chains of pairs
 #pragma unroll
     for (int kk = 0; kk < NV; ++kk) {
-      // Branch-free: a thread past the row's end reads the last vector and
-      // zeroes it.
-      const int v = kk * T + tid;
-      const bool act = v < nvec;
-      const uint4 r = *reinterpret_cast<const uint4*>(xs + (act ? v : nvec - 1) * VEC);
-      const uint32_t w[NW] = {act ? r.x : 0u, act ? r.y : 0u, act ? r.z : 0u, act ? r.w : 0u};
+      const uint4 r = *reinterpret_cast<const uint4*>(xs + kk * T * 16);
+      const uint32_t w[NW] = {r.x, r.y, r.z, r.w};
       widen_pairs<Tin, VEC>(w, xp[kk]);
 #pragma unroll
       for (int i = 0; i < NP; ++i) {
@@ -139,13 +175,21 @@ __global__ void __launch_bounds__(fwd_ring_max_threads(NV)) fwd_ring_kernel(cons
     // The barrier of the first reduction also tells thread 0 that every
     // thread has copied its vectors out of this stage.
     if (nwarps == 1) __syncthreads();
-    s1 = block_sum(s1, red[rb], lane, warp, nwarps);
+    s1 = row_block_sum(s1, red[rb], lane, warp, nwarps);
     rb ^= 1;
     if (s_abort) break;
     if (tid == 0 && issued < sched.count) {
       mbar_arrive_expect_tx(&full[st], row_bytes);
-      bulk_g2s(ring + st * stage_bytes, x + sched.row(issued) * H, row_bytes, &full[st]);
+      bulk_g2s(ring + st * stage_bytes, src, row_bytes, &full[st]);
       ++issued;
+      src += row_step;
+    }
+    if (++st == stages) {
+      st = 0;
+      phase ^= 1u;
+      xs = ring + tid * 16;
+    } else {
+      xs += stage_bytes;
     }
     float mean = 0.f, ss = s1;
     if constexpr (LN) {
@@ -163,12 +207,13 @@ __global__ void __launch_bounds__(fwd_ring_max_threads(NV)) fwd_ring_kernel(cons
         }
       }
       const float2 qq = u2(add2(q0, q1));
-      ss = block_sum(qq.x + qq.y, red[rb], lane, warp, nwarps);
+      ss = row_block_sum(qq.x + qq.y, red[rb], lane, warp, nwarps);
       rb ^= 1;
     }
     const float rs = rsqrtf(fmaf(ss, inv_h, p.eps));
     const uint64_t rs2 = p2(rs, rs);
     if (tid == 0) {
+      const int64_t row = sched.row(k);
       if (LN && p.mu) p.mu[row] = mean;
       if (p.rsigma) p.rsigma[row] = rs;
     }
@@ -183,12 +228,12 @@ __global__ void __launch_bounds__(fwd_ring_max_threads(NV)) fwd_ring_kernel(cons
         const uint64_t t = mul2(xp[kk][i], rs2);
         z[i] = LN ? fma2(t, gw[kk][i], bw[kk][i]) : mul2(t, gw[kk][i]);
       }
-      const int64_t off = row * H + static_cast<int64_t>(v) * VEC;
+      Tout* o = orow + kk * vstep;
       if constexpr (QM == Q_NONE) {
         if (act) {
           uint32_t w[NW];
           narrow_pairs<Tin, VEC>(z, w);
-          st_words<NW>(reinterpret_cast<Tin*>(p.out) + off, w);
+          st_words<NW>(o, w);
         }
       } else {
         float a = 0.f;
@@ -204,7 +249,7 @@ __global__ void __launch_bounds__(fwd_ring_max_threads(NV)) fwd_ring_kernel(cons
         } else {  // MXFP8 rowwise: 32-element blocks span 32/VEC adjacent threads
           constexpr int TPB = 32 / VEC;
 #pragma unroll
-          for (int o = 1; o < TPB; o <<= 1) a = fmax_nan(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+          for (int o2 = 1; o2 < TPB; o2 <<= 1) a = fmax_nan(a, __shfl_xor_sync(0xFFFFFFFFu, a, o2));
           code = e8m0_code(a);
           const float m = e8m0_mult(code);
           s2 = p2(m, m);
@@ -213,11 +258,11 @@ __global__ void __launch_bounds__(fwd_ring_max_threads(NV)) fwd_ring_kernel(cons
           uint32_t w[VEC / 4];
 #pragma unroll
           for (int i = 0; i < VEC / 4; ++i) w[i] = e4m3x4_pairs(z[2 * i], z[2 * i + 1], s2);
-          st_words<VEC / 4>(reinterpret_cast<uint8_t*>(p.out) + off, w);
+          st_words<VEC / 4>(o, w);
           if constexpr (QM == Q_MXFP8) {
             constexpr int TPB = 32 / VEC;
             if ((tid & (TPB - 1)) == 0)
-              p.mx_scale[row * (H / 32) + (v * VEC) / 32] = static_cast<uint8_t>(code);
+              p.mx_scale[sched.row(k) * (H / 32) + (v * VEC) / 32] = static_cast<uint8_t>(code);
           }
         }
       }
