@@ -10,9 +10,11 @@
 // written, and 32 rows of a long row do not fit one SM.  A thread-block
 // cluster of C CTAs therefore takes one 32-row stripe: CTA `rank` owns
 // columns [rank*hc, (rank+1)*hc).
-//   1. The CTA's 32 x hc slice arrives in shared memory by bulk copies (the
-//      next slice is prefetched into L2, and with two stages already copied,
-//      while this one is processed).
+//   1. The CTA's 32 x hc slice arrives in shared memory by bulk copies (with
+//      two stages, the next slice is copied while this one is processed; with
+//      one, the other CTAs on the SM keep it busy meanwhile).  No L2
+//      prefetch of the next slice: measured, its lines were often evicted
+//      before use and read twice.
 //   2. One warp per four rows reduces the slice's per-row mean and M2; the 32
 //      pairs are pushed to every CTA of the cluster with `st.async`, whose
 //      bytes complete a transaction count on the receiver's mbarrier.  Every
@@ -154,8 +156,6 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
     const int b = stages == 2 ? static_cast<int>(k & 1) : 0;
     const uint32_t par = static_cast<uint32_t>(stages == 2 ? (k >> 1) & 1 : k & 1);
     const int sb = static_cast<int>(k & 1);  // stat buffer
-    if (tid < kStripeRows && k + stages < count)
-      prefetch_l2(x + (stripe_of(k + stages) * kStripeRows + tid) * H + c0, row_bytes);
     if (tid == 0) mbar_arrive_expect_tx(&statbar[sb], C * kStripeRows * sizeof(float2));
     wait(&full[b], par, k);
     const Tin* xs = reinterpret_cast<const Tin*>(xbuf + b * slice);

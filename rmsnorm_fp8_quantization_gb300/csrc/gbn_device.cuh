@@ -38,12 +38,6 @@ __device__ __forceinline__ uint2 ld_cached8(const void* p) {
   return r;
 }
 
-// Fire-and-forget prefetch of a contiguous range into L2 by the bulk-copy
-// engine (address 16-byte aligned, size a multiple of 16).
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 // ---------------------------------------------------------------- element types
 
 template <typename T> struct Elem;
