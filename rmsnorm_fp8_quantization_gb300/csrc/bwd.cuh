@@ -20,6 +20,7 @@ namespace gbn {
 // one thread each, so no synchronization is needed on them).
 template <typename Tin>
 __global__ void __launch_bounds__(256) bwd_generic_kernel(const BwdParams p) {
+  pdl_begin();
   __shared__ float2 red[2][32];
   const int tid = threadIdx.x, T = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5, nwarps = T >> 5;

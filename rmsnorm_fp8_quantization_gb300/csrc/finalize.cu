@@ -12,6 +12,7 @@ constexpr int kFinWarps = 32;
 constexpr int kFinCols = 32;
 
 __global__ void __launch_bounds__(kFinWarps * 32) bwd_finalize_kernel(const FinalizeParams p) {
+  pdl_begin();
   __shared__ float acc[kFinWarps][32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float* part = blockIdx.y == 0 ? p.part_dgamma : p.part_dbeta;
@@ -42,8 +43,7 @@ __global__ void __launch_bounds__(kFinWarps * 32) bwd_finalize_kernel(const Fina
 
 cudaError_t launch_bwd_finalize(const FinalizeParams& p, cudaStream_t stream) {
   const dim3 grid((p.hidden + kFinCols - 1) / kFinCols, p.part_dbeta ? 2 : 1, 1);
-  bwd_finalize_kernel<<<grid, kFinWarps * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(bwd_finalize_kernel, grid, dim3(kFinWarps * 32), 0, stream, p);
 }
 
 }  // namespace gbn

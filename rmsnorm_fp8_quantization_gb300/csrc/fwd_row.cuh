@@ -29,6 +29,7 @@ __device__ __forceinline__ float z_at(const FwdParams& p, int64_t row, int j, fl
 // interface accepts; the vectorized kernels cover the fast cases.
 template <typename Tin, int QM>
 __global__ void __launch_bounds__(256) fwd_generic_kernel(const FwdParams p) {
+  pdl_begin();
   __shared__ float s_mean[32], s_rs[32], red[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int H = p.hidden;

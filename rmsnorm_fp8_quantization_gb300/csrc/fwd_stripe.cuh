@@ -77,6 +77,7 @@ __device__ __forceinline__ void transpose4x4(const uint32_t* in, uint32_t* out) 
 template <typename Tin, int QM, bool LN>
 __global__ void __launch_bounds__(kStripeThreads, 3)
     fwd_stripe_kernel(const FwdParams p, const int hc, const int stages) {
+  pdl_begin();
   constexpr int VEC = 16 / (int)sizeof(Tin);
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint64_t full[2];                          // x slice landed

@@ -399,6 +399,16 @@ __device__ __forceinline__ void block_amax_commit(float v, float* buf, float* am
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+// Programmatic dependent launch.  Every kernel of the library first lets the
+// next kernel of the stream begin launching (its CTAs take SMs as this
+// grid's CTAs leave), then waits until the previous kernel has completed and
+// its writes are visible, before touching global memory.  Without the launch
+// attribute both are no-ops.
+__device__ __forceinline__ void pdl_begin() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

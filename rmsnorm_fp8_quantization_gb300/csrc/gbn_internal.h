@@ -9,6 +9,26 @@
 
 namespace gbn {
 
+// Launches `k` with programmatic dependent launch allowed: it may begin
+// launching while the previous kernel of the stream finishes; the kernels
+// order their global-memory accesses with griddepcontrol (pdl_begin).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k, args...);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 enum Dt : int { DT_F32 = 0, DT_BF16 = 1, DT_F16 = 2 };
 enum Qm : int { Q_NONE = 0, Q_DELAYED = 1, Q_MXFP8 = 2 };
 

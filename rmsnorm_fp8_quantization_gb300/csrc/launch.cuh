@@ -28,15 +28,13 @@ struct Launch {
   static cudaError_t fwd_generic_launch(int qm, const FwdParams& p, int grid, cudaStream_t st) {
     Kfwd k = fwd_generic(qm);
     if (!k) return cudaErrorInvalidValue;
-    k<<<grid, 256, 0, st>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(k, dim3(grid), dim3(256), 0, st, p);
   }
   static cudaError_t bwd_generic_occupancy(int* occ) {
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, bwd_generic_kernel<Tin>, 256, 0);
   }
   static cudaError_t bwd_generic_launch(const BwdParams& p, int grid, cudaStream_t st) {
-    bwd_generic_kernel<Tin><<<grid, 256, 0, st>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(bwd_generic_kernel<Tin>, dim3(grid), dim3(256), 0, st, p);
   }
 
   using Kstripe3 = void (*)(const FwdParams, const int, const int);
@@ -47,12 +45,15 @@ struct Launch {
                                  : fwd_stripe_kernel<Tin, Q_MXFP8, false>;
     return nullptr;
   }
+  // attr[0]: cluster shape; attr[1] (launches only): programmatic dependent launch
   static void stripe_config(const StripeGeom& g, int nclusters, cudaLaunchConfig_t* cfg,
                             cudaLaunchAttribute* attr) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(g.cluster);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     *cfg = cudaLaunchConfig_t{};
     cfg->gridDim = dim3(static_cast<unsigned>(nclusters * g.cluster), 1, 1);
     cfg->blockDim = dim3(kStripeThreads, 1, 1);
@@ -66,7 +67,7 @@ struct Launch {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     stripe_config(g, 1024 / g.cluster, &cfg, attr);
     return cudaOccupancyMaxActiveClusters(n, k, &cfg);
   }
@@ -77,8 +78,9 @@ struct Launch {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     stripe_config(g, nclusters, &cfg, attr);
+    cfg.numAttrs = 2;
     cfg.stream = st;
     e = cudaLaunchKernelEx(&cfg, k, p, g.hc, g.stages);
     if (e != cudaSuccess) return e;
@@ -145,8 +147,7 @@ struct Launch {
     if (!k) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    k<<<grid, g.threads, smem, st>>>(p, stages);
-    return cudaGetLastError();
+    return launch_pdl(k, dim3(grid), dim3(g.threads), smem, st, p, stages);
   }
   static cudaError_t bwd_ring_occupancy(bool ln, bool add, const RowGeom& g, int smem, int* occ) {
     Kbring k = bwd_ring(ln, add, g.nv);
@@ -158,8 +159,7 @@ struct Launch {
     if (!k) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    k<<<grid, g.threads, smem, st>>>(p, stages);
-    return cudaGetLastError();
+    return launch_pdl(k, dim3(grid), dim3(g.threads), smem, st, p, stages);
   }
   static cudaError_t read_device_error(unsigned int* v, bool clear) {
     cudaError_t e = cudaMemcpyFromSymbol(v, g_gbn_device_error, sizeof(unsigned int));

@@ -95,6 +95,7 @@ __device__ __forceinline__ float row_block_sum(float v, float* buf, int lane, in
 template <typename Tin, int QM, bool LN, int NV>
 __global__ void __launch_bounds__(fwd_ring_max_threads(NV)) fwd_ring_kernel(const FwdParams p,
                                                                            const int stages) {
+  pdl_begin();
   constexpr int VEC = 16 / (int)sizeof(Tin);
   constexpr int NW = Words<Tin, VEC>::n;
   constexpr int NP = VEC / 2;
@@ -295,6 +296,7 @@ __global__ void __launch_bounds__(fwd_ring_max_threads(NV)) fwd_ring_kernel(cons
 template <typename Tin, bool LN, bool ADD, int NV>
 __global__ void __launch_bounds__(bwd_max_threads(NV)) bwd_ring_kernel(const BwdParams p,
                                                                       const int stages) {
+  pdl_begin();
   constexpr int VEC = 16 / (int)sizeof(Tin);
   constexpr int NW = Words<Tin, VEC>::n;
   constexpr int NP = VEC / 2;
