@@ -6,8 +6,9 @@ result meaningless):
   * fp32 results: |got - ref| <= 1e-5 |ref| + 8 * 2^-24 * T
   * bf16 / f16 results: |got - ref| <= 1 ulp(ref) + 8 * 2^-24 * T
     where T is the magnitude of the terms the kernel adds in fp32
-    (for z: |x - mu| rsigma |g'| + |beta|; for dx: rsigma (|dy| + |c1| +
-    |xhat c2|) + |dresidual|).
+    (for z: |x - mu| rsigma |g'| + |beta|; for dx: rsigma (|dy| +
+    mean|dy| + |xhat| mean|dy xhat|) + |dresidual|, the summands of c1 =
+    mean(dy) and c2 = mean(dy xhat) standing for their fp32 error).
   * mu / rsigma: rel 1e-4 (plus the same fp32 term bound for mu).
   * dgamma / dbeta: rel 1e-4 plus 1e-6 * sum_i |term_i| (fp32 partial sums
     over all rows; far below one row's contribution, so a dropped or doubled
@@ -141,9 +142,12 @@ def bwd_terms(dz, x, mu, rs, gamma, dres, norm, zcg):
     rs64 = np.asarray(rs, np.float64)
     xh = (xd - mu64[:, None]) * rs64[:, None]
     dy = dzd * g[None, :]
-    c1 = dy.mean(1, keepdims=True) if norm == 0 else 0.0
-    c2 = (dy * xh).mean(1, keepdims=True)
-    t_dx = rs64[:, None] * (np.abs(dy) + np.abs(c1) + np.abs(xh * c2))
+    # c1 = mean(dy) and c2 = mean(dy * xhat) are fp32 sums: their evaluation
+    # error scales with the magnitude of their summands, not with |c1|, |c2|
+    # (which cancellation can make arbitrarily small).
+    m1 = np.abs(dy).mean(1, keepdims=True) if norm == 0 else 0.0
+    m2 = np.abs(dy * xh).mean(1, keepdims=True)
+    t_dx = rs64[:, None] * (np.abs(dy) + m1 + np.abs(xh) * m2)
     if dres is not None:
         t_dx = t_dx + np.abs(to64(dres))
     t_dg = np.abs(dzd * xh).sum(0)
