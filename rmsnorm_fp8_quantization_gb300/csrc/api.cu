@@ -181,6 +181,115 @@ RingChoice choose_ring(int key_kind, int in, const RowGeom& g, int stage_bytes, 
   return best;
 }
 
+// Long rows: the smallest cluster C (2..8) whose per-CTA slice hc = H / C
+// fits the cluster forward kernel (kClusterFwdNv vectors per thread, at most
+// fwd_ring_max_threads(kClusterFwdNv) threads; MXFP8 slices whole 32-blocks),
+// then the stage count that puts the most bytes in flight (up to the ring
+// target per SM), ties to more resident clusters.  Cached.
+struct ClusterChoice {
+  int cluster = 0, threads = 0, hc = 0, stages = 0, stage_bytes = 0, max_clusters = 0;
+};
+
+bool cluster_fwd_geom(const KernelTable& kt, int in, int kind, int qm, int64_t hidden, int vec,
+                      int sms, ClusterChoice* out) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int, int64_t>, std::pair<bool, ClusterChoice>> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const auto key = std::make_tuple(dev, in, kind, hidden);
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+      *out = it->second.second;
+      return it->second.first;
+    }
+  }
+  constexpr int64_t kTarget = 224 * 1024;
+  ClusterChoice best;
+  bool found = false;
+  for (int c = 2; c <= 8 && !found; ++c) {
+    if (hidden % (static_cast<int64_t>(c) * vec)) continue;
+    const int64_t hc = hidden / c;
+    if (qm == Q_MXFP8 && hc % 32) continue;
+    const int64_t nvc = hc / vec;
+    const int64_t t = ((nvc + kClusterFwdNv - 1) / kClusterFwdNv + 31) / 32 * 32;
+    if (t > fwd_ring_max_threads(kClusterFwdNv)) continue;
+    const int stage_bytes = ring_slot_bytes(kClusterFwdNv, static_cast<int>(t));
+    int64_t best_inflight = -1;
+    for (int st = 1; st <= kMaxRingStagesHost; ++st) {
+      const int smem = st * stage_bytes;
+      if (smem > kMaxSmemPerCta) break;
+      int n = 0;
+      if (kt.fwd_cluster_max_clusters(kind, c, static_cast<int>(t), smem, &n) != cudaSuccess ||
+          n < 1)
+        continue;
+      int64_t inflight = static_cast<int64_t>(n) * c * (st > 1 ? st - 1 : 1) * stage_bytes / sms;
+      if (inflight > kTarget) inflight = kTarget;
+      if (inflight > best_inflight || (inflight == best_inflight && n > best.max_clusters)) {
+        best_inflight = inflight;
+        best = ClusterChoice{c, static_cast<int>(t), static_cast<int>(hc), st, stage_bytes, n};
+        found = true;
+      }
+    }
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  cache[key] = std::make_pair(found, best);
+  *out = best;
+  return found;
+}
+
+// Long rows, backward: as cluster_fwd_geom with kClusterBwdNv vectors per
+// thread, at most bwd_max_threads(kClusterBwdNv) threads and 4 stages of
+// (dz, x[, dresidual]) slices.  Cached.
+bool cluster_bwd_geom(const KernelTable& kt, int in, bool ln, bool add, int64_t hidden, int vec,
+                      int sms, ClusterChoice* out) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int, int, int64_t>, std::pair<bool, ClusterChoice>> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const auto key = std::make_tuple(dev, in, ln ? 1 : 0, add ? 1 : 0, hidden);
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+      *out = it->second.second;
+      return it->second.first;
+    }
+  }
+  constexpr int64_t kTarget = 224 * 1024;
+  ClusterChoice best;
+  bool found = false;
+  for (int c = 2; c <= 8 && !found; ++c) {
+    if (hidden % (static_cast<int64_t>(c) * vec)) continue;
+    const int64_t hc = hidden / c;
+    const int64_t nvc = hc / vec;
+    const int64_t t = ((nvc + kClusterBwdNv - 1) / kClusterBwdNv + 31) / 32 * 32;
+    if (t > bwd_max_threads(kClusterBwdNv)) continue;
+    const int stage_bytes = (add ? 3 : 2) * ring_slot_bytes(kClusterBwdNv, static_cast<int>(t));
+    int64_t best_inflight = -1;
+    for (int st = 1; st <= 4; ++st) {
+      const int smem = st * stage_bytes;
+      if (smem > kMaxSmemPerCta) break;
+      int n = 0;
+      if (kt.bwd_cluster_max_clusters(ln, add, c, static_cast<int>(t), smem, &n) != cudaSuccess ||
+          n < 1)
+        continue;
+      int64_t inflight = static_cast<int64_t>(n) * c * (st > 1 ? st - 1 : 1) * stage_bytes / sms;
+      if (inflight > kTarget) inflight = kTarget;
+      if (inflight > best_inflight || (inflight == best_inflight && n > best.max_clusters)) {
+        best_inflight = inflight;
+        best = ClusterChoice{c, static_cast<int>(t), static_cast<int>(hc), st, stage_bytes, n};
+        found = true;
+      }
+    }
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  cache[key] = std::make_pair(found, best);
+  *out = best;
+  return found;
+}
+
 gbn_status check_fwd_args(int64_t rows, int64_t hidden, gbn_dtype in, gbn_dtype w, gbn_dtype out,
                           gbn_norm_type norm, gbn_scaling_mode sc, gbn_quantize_layout lay) {
   if (norm != GBN_LAYERNORM && norm != GBN_RMSNORM) return GBN_ERR_ENUM;
@@ -231,11 +340,24 @@ gbn_status plan_bwd(int64_t rows, int64_t hidden, gbn_dtype in, gbn_norm_type no
       if (rc.stages >= 1 && rc.occ > occ) occ = rc.occ;
     }
   }
+  // Long rows: clusters (P = clusters; the generic fallback stays within P).
+  int64_t cl_parts = 0;
+  if (g.vec == 1 && hidden % vec == 0) {
+    for (int add = 0; add < 2; ++add) {
+      ClusterChoice cc;
+      if (cluster_bwd_geom(kt, in, ln, add != 0, hidden, vec, sms, &cc)) {
+        const int64_t n = static_cast<int64_t>(static_cast<double>(cc.max_clusters) *
+                                               effective_sms(sms, sm_margin) / sms);
+        if (n > cl_parts) cl_parts = n;
+      }
+    }
+    if (cl_parts >= 1) occ = 1;
+  }
   if (occ < 1) {
     if (kt.bwd_generic_occupancy(&occ) != cudaSuccess) return GBN_ERR_CUDA;
     if (occ < 1) occ = 1;
   }
-  int64_t parts = static_cast<int64_t>(effective_sms(sms, sm_margin)) * occ;
+  int64_t parts = cl_parts >= 1 ? cl_parts : static_cast<int64_t>(effective_sms(sms, sm_margin)) * occ;
   if (parts > rows) parts = rows;
   if (parts < 1) parts = 1;
   plan->geom = g;
@@ -380,6 +502,18 @@ gbn_status gbn_norm_fwd(const void* x, const void* gamma, const void* beta, cons
       return e == cudaSuccess ? GBN_OK : GBN_ERR_CUDA;
     }
   }
+  ClusterChoice cc;
+  if (vec_ok && rows > 0 &&
+      cluster_fwd_geom(kt, in_dtype, qm * 2 + (ln ? 1 : 0), qm, hidden, vec, sms, &cc)) {
+    // Rows longer than one CTA's ring: each row split over a cluster.
+    int64_t ncl = static_cast<int64_t>(static_cast<double>(cc.max_clusters) * esms / sms);
+    if (ncl > rows) ncl = rows;
+    if (ncl < 1) ncl = 1;
+    const cudaError_t e = kt.fwd_cluster_launch(qm * 2 + (ln ? 1 : 0), cc.cluster, cc.threads,
+                                                cc.stages, cc.stages * cc.stage_bytes, cc.hc, p,
+                                                static_cast<int>(ncl), stream);
+    return e == cudaSuccess ? GBN_OK : GBN_ERR_CUDA;
+  }
   // Generic kernel: persistent over 32-row stripes.
   int occ = 0;
   if (kt.fwd_generic_occupancy(qm, &occ) != cudaSuccess) return GBN_ERR_CUDA;
@@ -442,12 +576,20 @@ gbn_status gbn_norm_bwd(const void* dz, const void* x, const float* mu, const fl
   if (g.vec != 1) rc = bwd_ring_choice(kt, in_dtype, ln, add, g, hidden, &stage_bytes);
   int occ = rc.occ;
   const bool ring = rc.stages >= 1;
+  // Long rows: each row over a cluster, when the pointers allow vectors.
+  ClusterChoice cc;
+  const bool cluster = !ring && plan.geom.vec == 1 && hidden % vec == 0 && rows > 0 &&
+                       aligned(dz, 16) && aligned(x, 16) && aligned(dx, 16) &&
+                       (!dresidual || aligned(dresidual, 16)) && aligned(gamma, walign) &&
+                       cluster_bwd_geom(kt, in_dtype, ln, add, hidden, vec, sms, &cc);
   if (!ring) {
     g = generic_geom();
     if (kt.bwd_generic_occupancy(&occ) != cudaSuccess) return GBN_ERR_CUDA;
   }
   int64_t grid = static_cast<int64_t>(esms) * (occ > 0 ? occ : 1);
+  if (cluster) grid = static_cast<int64_t>(static_cast<double>(cc.max_clusters) * esms / sms);
   if (grid > plan.parts) grid = plan.parts;
+  if (grid > rows && cluster) grid = rows;
   if (grid < 1) grid = 1;
 
   float* ws = static_cast<float*>(workspace);
@@ -467,9 +609,12 @@ gbn_status gbn_norm_bwd(const void* dz, const void* x, const float* mu, const fl
   p.zcg = zero_centered_gamma ? 1 : 0;
   p.w_dt = w_dtype == GBN_F32 ? DT_F32 : (w_dtype == GBN_BF16 ? DT_BF16 : DT_F16);
   const cudaError_t le =
-      ring ? kt.bwd_ring_launch(ln, add, g, rc.stages, rc.stages * stage_bytes, p,
-                                static_cast<int>(grid), stream)
-           : kt.bwd_generic_launch(p, static_cast<int>(grid), stream);
+      ring      ? kt.bwd_ring_launch(ln, add, g, rc.stages, rc.stages * stage_bytes, p,
+                                     static_cast<int>(grid), stream)
+      : cluster ? kt.bwd_cluster_launch(ln, add, cc.cluster, cc.threads, cc.stages,
+                                        cc.stages * cc.stage_bytes, cc.hc, p,
+                                        static_cast<int>(grid), stream)
+                : kt.bwd_generic_launch(p, static_cast<int>(grid), stream);
   if (le != cudaSuccess) return GBN_ERR_CUDA;
 
   FinalizeParams f = {};

@@ -39,17 +39,6 @@ constexpr int kStripeWarps = kStripeThreads / 32;
 constexpr int kRowsPerWarp = kStripeRows / kStripeWarps;  // 4
 constexpr int kMaxCluster = 8;
 
-// Pushes v into element `buf` of CTA `rank` of this cluster and reports
-// 8 bytes on that CTA's mbarrier `bar` (same offsets in every CTA).
-__device__ __forceinline__ void push_stat(float2* buf, uint64_t* bar, uint32_t rank, float2 v) {
-  uint32_t ra, rb;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(buf)), "r"(rank));
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_u32(bar)), "r"(rank));
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
-               ::"r"(ra), "f"(v.x), "f"(v.y), "r"(rb)
-               : "memory");
-}
-
 // Four consecutive elements of a shared-memory row as two fp32 pairs.
 template <typename Tin>
 __device__ __forceinline__ void lds4_pairs(const Tin* p, uint64_t* pr) {

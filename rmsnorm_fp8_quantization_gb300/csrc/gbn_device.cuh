@@ -484,6 +484,17 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
                ::: "memory");
 }
+// Pushes v into element `buf` of CTA `rank` of this cluster and reports
+// 8 bytes on that CTA's mbarrier `bar` (same offsets in every CTA).
+__device__ __forceinline__ void push_stat(float2* buf, uint64_t* bar, uint32_t rank, float2 v) {
+  uint32_t ra, rb;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(buf)), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_u32(bar)), "r"(rank));
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+               ::"r"(ra), "f"(v.x), "f"(v.y), "r"(rb)
+               : "memory");
+}
+
 // Reads a float2 from the shared memory of CTA `rank` of this cluster at the
 // address that `local` has in this CTA.
 __device__ __forceinline__ float2 dsmem_ld2(const float2* local, uint32_t rank) {

@@ -150,9 +150,27 @@ struct KernelTable {
                                     int* blocks_per_sm);
   cudaError_t (*bwd_ring_launch)(bool layernorm, bool add, const RowGeom& g, int stages, int smem,
                                  const BwdParams& p, int grid, cudaStream_t stream);
+  // Long rows: forward with each row split over a cluster of `cluster` CTAs
+  // of `threads` threads (4 vectors per thread), each owning hc columns.
+  cudaError_t (*fwd_cluster_max_clusters)(int kind, int cluster, int threads, int smem,
+                                          int* clusters);
+  cudaError_t (*fwd_cluster_launch)(int kind, int cluster, int threads, int stages, int smem,
+                                    int hc, const FwdParams& p, int clusters,
+                                    cudaStream_t stream);
+  // Long rows: backward with each row split over a cluster (2 vectors per
+  // thread); partials go to workspace row `cluster id`.
+  cudaError_t (*bwd_cluster_max_clusters)(bool layernorm, bool add, int cluster, int threads,
+                                          int smem, int* clusters);
+  cudaError_t (*bwd_cluster_launch)(bool layernorm, bool add, int cluster, int threads,
+                                    int stages, int smem, int hc, const BwdParams& p,
+                                    int clusters, cudaStream_t stream);
   // Sticky device-side error bits of this translation unit's kernels.
   cudaError_t (*read_device_error)(unsigned int* value, bool clear);
 };
+
+// Vectors per thread of the long-row (cluster) kernels.
+constexpr int kClusterFwdNv = 4;
+constexpr int kClusterBwdNv = 2;
 
 const KernelTable& kernels_f32();
 const KernelTable& kernels_bf16();

@@ -4,6 +4,7 @@
 #pragma once
 
 #include "bwd.cuh"
+#include "cluster_row.cuh"
 #include "fwd_row.cuh"
 #include "fwd_stripe.cuh"
 #include "ring.cuh"
@@ -161,6 +162,96 @@ struct Launch {
     if (e != cudaSuccess) return e;
     return launch_pdl(k, dim3(grid), dim3(g.threads), smem, st, p, stages);
   }
+  // ---- long rows: a row split over a thread-block cluster
+  using Kcl = void (*)(const FwdParams, const int, const int);
+  static Kcl fwd_cluster(int kind) {
+    constexpr int NV = kClusterFwdNv;
+    switch (kind) {
+      case 0: return fwd_cluster_kernel<Tin, Q_NONE, false, NV>;
+      case 1: return fwd_cluster_kernel<Tin, Q_NONE, true, NV>;
+      case 2: return fwd_cluster_kernel<Tin, Q_DELAYED, false, NV>;
+      case 3: return fwd_cluster_kernel<Tin, Q_DELAYED, true, NV>;
+      case 4: return fwd_cluster_kernel<Tin, Q_MXFP8, false, NV>;
+      case 5: return fwd_cluster_kernel<Tin, Q_MXFP8, true, NV>;
+      default: return nullptr;
+    }
+  }
+  // attr[0]: cluster shape; attr[1] (launches only): programmatic dependent launch
+  static void cluster_config(int cluster, int nclusters, int threads, int smem,
+                             cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    *cfg = cudaLaunchConfig_t{};
+    cfg->gridDim = dim3(static_cast<unsigned>(nclusters * cluster), 1, 1);
+    cfg->blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+    cfg->dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg->attrs = attr;
+    cfg->numAttrs = 1;
+  }
+  static cudaError_t fwd_cluster_max_clusters(int kind, int cluster, int threads, int smem,
+                                              int* n) {
+    Kcl k = fwd_cluster(kind);
+    if (!k) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    cluster_config(cluster, 1024 / cluster, threads, smem, &cfg, attr);
+    return cudaOccupancyMaxActiveClusters(n, k, &cfg);
+  }
+  static cudaError_t fwd_cluster_launch(int kind, int cluster, int threads, int stages, int smem,
+                                        int hc, const FwdParams& p, int nclusters,
+                                        cudaStream_t st) {
+    Kcl k = fwd_cluster(kind);
+    if (!k) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    cluster_config(cluster, nclusters, threads, smem, &cfg, attr);
+    cfg.numAttrs = 2;
+    cfg.stream = st;
+    e = cudaLaunchKernelEx(&cfg, k, p, stages, hc);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  }
+
+  using Kbcl = void (*)(const BwdParams, const int, const int);
+  static Kbcl bwd_cluster(bool ln, bool add) {
+    constexpr int NV = kClusterBwdNv;
+    if (ln) return add ? bwd_cluster_kernel<Tin, true, true, NV> : bwd_cluster_kernel<Tin, true, false, NV>;
+    return add ? bwd_cluster_kernel<Tin, false, true, NV> : bwd_cluster_kernel<Tin, false, false, NV>;
+  }
+  static cudaError_t bwd_cluster_max_clusters(bool ln, bool add, int cluster, int threads,
+                                              int smem, int* n) {
+    Kbcl k = bwd_cluster(ln, add);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    cluster_config(cluster, 1024 / cluster, threads, smem, &cfg, attr);
+    return cudaOccupancyMaxActiveClusters(n, k, &cfg);
+  }
+  static cudaError_t bwd_cluster_launch(bool ln, bool add, int cluster, int threads, int stages,
+                                        int smem, int hc, const BwdParams& p, int nclusters,
+                                        cudaStream_t st) {
+    Kbcl k = bwd_cluster(ln, add);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    cluster_config(cluster, nclusters, threads, smem, &cfg, attr);
+    cfg.numAttrs = 2;
+    cfg.stream = st;
+    e = cudaLaunchKernelEx(&cfg, k, p, stages, hc);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  }
+
   static cudaError_t read_device_error(unsigned int* v, bool clear) {
     cudaError_t e = cudaMemcpyFromSymbol(v, g_gbn_device_error, sizeof(unsigned int));
     if (e != cudaSuccess || !clear) return e;

@@ -1,0 +1,51 @@
+"""Rows longer than one CTA's ring (over 16384 two-byte or 8192 four-byte
+elements): the forward splits each row over a thread-block cluster and
+combines the row statistics across it; the backward does the same.  Parity
+with the oracle, as for the short rows, including slices with a ragged tail
+and every rowwise output kind."""
+import dataclasses
+
+import pytest
+
+from rmsnorm_fp8_quantization_gb300.workloads import WORKLOADS
+from test_gpu_parity import run_bwd_and_check, run_fwd_and_check
+
+pytestmark = pytest.mark.gpu
+
+
+def wl(name, rows, hidden, **kw):
+    return dataclasses.replace(WORKLOADS[name].with_shape(rows, hidden), **kw)
+
+
+FWD = [
+    ("ln 32768", wl("ln_bf16_16384x4096", 37, 32768)),
+    ("ln f16 zcg ragged slice 20000", wl("ln_bf16_16384x4096", 19, 20000, in_dtype="f16",
+                                          w_dtype="f16", zero_centered_gamma=True)),
+    ("rms 65536", wl("rms_bwd_add_bf16_32768x12288", 33, 65536, passes=("fwd",))),
+    ("rms f32 12288", wl("rms_f32_64x1024", 20, 12288)),
+    ("rms f32 24576 many clusters", wl("rms_f32_64x1024", 301, 24576)),
+    ("delayed rowwise 40960", wl("rms_bf16_e4m3_delayed_32768x8192", 40, 40960,
+                                 layout="rowwise")),
+    ("mxfp8 rowwise 49152", wl("rms_bf16_mxfp8_16384x5120", 32, 49152, layout="rowwise")),
+    ("ln mxfp8 rowwise 36864", wl("rms_bf16_mxfp8_16384x5120", 24, 36864, layout="rowwise",
+                                  norm="layernorm")),
+]
+
+
+@pytest.mark.parametrize("label,w", FWD, ids=[f[0] for f in FWD])
+def test_long_row_forward(gpu, label, w):
+    run_fwd_and_check(gpu, w)
+
+
+BWD = [
+    ("ln 32768", wl("ln_bf16_16384x4096", 37, 32768)),
+    ("rms add 65536", wl("rms_bwd_add_bf16_32768x12288", 21, 65536)),
+    ("ln add f16 ragged 20000", wl("ln_bf16_16384x4096", 19, 20000, in_dtype="f16",
+                                    w_dtype="f16", dresidual=True)),
+    ("rms f32 12288", wl("rms_f32_64x1024", 20, 12288)),
+]
+
+
+@pytest.mark.parametrize("label,w", BWD, ids=[b[0] for b in BWD])
+def test_long_row_backward(gpu, label, w):
+    run_bwd_and_check(gpu, w)
