@@ -69,11 +69,24 @@ typedef enum {
 } gbn_scaling_mode;
 
 /* Which quantized outputs are written (the page's JAXX_Quantize_Layout:
- * rowwise, columnwise, or both).  Ignored when the scaling mode is NONE. */
+ * rowwise, columnwise, or both).  Ignored when the scaling mode is NONE.
+ *
+ * GBN_LAYOUT_SWIZZLED_SCALES may be OR-ed into the layout with MXFP8 (no
+ * counterpart on the pages; else GBN_ERR_ENUM).  The E8M0 scales then go to
+ * padded buffers in the tiled order that block-scaled GEMMs read: a scale
+ * matrix of R outer rows and B scales per row is padded to
+ * R' = roundup(R, 128) x B' = roundup(B, 4) and stored as 512-byte tiles of
+ * 128 x 4 scales, (R'/128) x (B'/4) tiles in row-major order; inside a tile,
+ * scale (r, c) is byte 16 * (r % 32) + 4 * (r / 32) + c.  Rowwise scales:
+ * R = rows, B = hidden/32 (row r, block b).  Columnwise scales: the operand
+ * is used transposed, R = hidden, B = rows/32 (column h, rows 32s..32s+31 is
+ * entry (h, s)).  Buffer sizes: R' * B' bytes.  Padding bytes are not
+ * written. */
 typedef enum {
   GBN_LAYOUT_ROWWISE = 0,
   GBN_LAYOUT_COLWISE = 1,
-  GBN_LAYOUT_ROWWISE_COLWISE = 2
+  GBN_LAYOUT_ROWWISE_COLWISE = 2,
+  GBN_LAYOUT_SWIZZLED_SCALES = 0x100
 } gbn_quantize_layout;
 
 /* Element types.  Inputs and weights: F32, BF16, F16.  Unquantized output:
@@ -122,8 +135,10 @@ gbn_status gbn_norm_fwd_workspace_size(int64_t rows, int64_t hidden, gbn_dtype i
  *   rsigma   fp32 [rows]; may be NULL (not written)
  *   scale_inv        delayed: fp32 [1] = 1/scale (rowwise layouts);
  *                    MXFP8: E8M0 [rows, hidden/32] rowwise block scales
+ *                    (tiled and padded with GBN_LAYOUT_SWIZZLED_SCALES)
  *   colwise_scale_inv  delayed: fp32 [1] = 1/scale (colwise layouts);
  *                    MXFP8: E8M0 [rows/32, hidden] columnwise block scales
+ *                    (tiled and padded with GBN_LAYOUT_SWIZZLED_SCALES)
  *   updated_amax     fp32 [1], delayed scaling: max |z| over the whole output
  *                    (before scaling; NaN propagates).  Zeroed on `stream` by
  *                    this call, then reduced into.

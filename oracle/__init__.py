@@ -214,6 +214,36 @@ def mxfp8_colwise(z: np.ndarray):
     return q, s
 
 
+def mxfp8_swizzle(s: np.ndarray):
+    """The padded, tiled GEMM order of an E8M0 scale matrix s [R, B] (R outer
+    rows, B scales per row), built tile by tile: R and B are padded to
+    R' = roundup(R, 128), B' = roundup(B, 4); the tiles of 128 rows x 4
+    scales follow each other in row-major order, 512 bytes each; a tile is 32
+    lines of 16 bytes, line i holding the 4 scales of rows i, i + 32, i + 64,
+    i + 96, in that order.  (The layout has no counterpart on the pages; it
+    is the order block-scaled GEMMs read.)
+
+    Returns (bytes [R' * B'] uint8, mask of the bytes that hold a scale)."""
+    s = np.asarray(s, dtype=np.uint8)
+    R, B = s.shape
+    Rp, Bp = (R + 127) // 128 * 128, (B + 3) // 4 * 4
+    out = np.zeros(Rp * Bp, dtype=np.uint8)
+    held = np.zeros(Rp * Bp, dtype=bool)
+    pos = 0
+    for tr in range(Rp // 128):
+        for tc in range(Bp // 4):
+            for line in range(32):
+                for quarter in range(4):
+                    r = tr * 128 + quarter * 32 + line
+                    for c4 in range(4):
+                        c = tc * 4 + c4
+                        if r < R and c < B:
+                            out[pos] = s[r, c]
+                            held[pos] = True
+                        pos += 1
+    return out, held
+
+
 def norm_bwd(dz, x, mu, rsigma, gamma, dresidual, norm: int, zero_centered_gamma: bool):
     """dx [rows, hidden], dgamma [hidden], dbeta [hidden] (float64).
 

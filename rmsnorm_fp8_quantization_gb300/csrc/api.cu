@@ -290,11 +290,18 @@ bool cluster_bwd_geom(const KernelTable& kt, int in, bool ln, bool add, int64_t 
   return found;
 }
 
+// The layout without the swizzled-scales flag.
+gbn_quantize_layout base_layout(gbn_quantize_layout lay) {
+  return static_cast<gbn_quantize_layout>(static_cast<int>(lay) & ~GBN_LAYOUT_SWIZZLED_SCALES);
+}
+
 gbn_status check_fwd_args(int64_t rows, int64_t hidden, gbn_dtype in, gbn_dtype w, gbn_dtype out,
-                          gbn_norm_type norm, gbn_scaling_mode sc, gbn_quantize_layout lay) {
+                          gbn_norm_type norm, gbn_scaling_mode sc, gbn_quantize_layout layout) {
   if (norm != GBN_LAYERNORM && norm != GBN_RMSNORM) return GBN_ERR_ENUM;
   if (sc < GBN_SCALING_NONE || sc > GBN_SCALING_MXFP8_1D) return GBN_ERR_ENUM;
+  const gbn_quantize_layout lay = base_layout(layout);
   if (lay < GBN_LAYOUT_ROWWISE || lay > GBN_LAYOUT_ROWWISE_COLWISE) return GBN_ERR_ENUM;
+  if (lay != layout && sc != GBN_SCALING_MXFP8_1D) return GBN_ERR_ENUM;
   if (!io_dtype(in) || !io_dtype(w)) return GBN_ERR_DTYPE;
   if (sc == GBN_SCALING_NONE ? out != in : out != GBN_E4M3) return GBN_ERR_DTYPE;
   if (rows < 0 || hidden < 1 || hidden > kMaxHidden) return GBN_ERR_SHAPE;
@@ -418,6 +425,8 @@ gbn_status gbn_norm_fwd(const void* x, const void* gamma, const void* beta, cons
   const bool ln = norm_type == GBN_LAYERNORM;
   const int qm = scaling_mode == GBN_SCALING_NONE ? Q_NONE
                  : scaling_mode == GBN_SCALING_DELAYED_TENSOR ? Q_DELAYED : Q_MXFP8;
+  const bool swizzle = base_layout(quantize_layout) != quantize_layout;
+  quantize_layout = base_layout(quantize_layout);
   const bool rowwise = qm == Q_NONE || quantize_layout != GBN_LAYOUT_COLWISE;
   const bool colwise = qm != Q_NONE && quantize_layout != GBN_LAYOUT_ROWWISE;
   // Row-sized buffers may be NULL only when there are no rows.
@@ -458,6 +467,7 @@ gbn_status gbn_norm_fwd(const void* x, const void* gamma, const void* beta, cons
   p.w_dt = w_dtype == GBN_F32 ? DT_F32 : (w_dtype == GBN_BF16 ? DT_BF16 : DT_F16);
   p.write_rowwise = rowwise ? 1 : 0;
   p.write_colwise = colwise ? 1 : 0;
+  p.mx_swizzle = swizzle ? 1 : 0;
 
   const int vec = 16 / esize(in_dtype);
   const uintptr_t walign = static_cast<uintptr_t>(vec * esize(w_dtype) < 16 ? vec * esize(w_dtype) : 16);

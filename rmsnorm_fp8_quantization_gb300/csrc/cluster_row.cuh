@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(fwd_ring_max_threads(NV))
           if constexpr (QM == Q_MXFP8) {
             constexpr int TPB = 32 / VEC;
             if ((tid & (TPB - 1)) == 0)
-              p.mx_scale[(cid + k * ncl) * (H / 32) + (c0 + v * VEC) / 32] =
+              p.mx_scale[mx_row_scale_at(p, cid + k * ncl, (c0 + v * VEC) / 32)] =
                   static_cast<uint8_t>(code);
           }
         }

@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(256) fwd_generic_kernel(const FwdParams p) {
           uint8_t* o = reinterpret_cast<uint8_t*>(p.out) + row * H + blk * 32;
           for (int e = 0; e < 32; ++e)
             o[e] = e4m3(z_at<Tin>(p, row, blk * 32 + e, s_mean[r], s_rs[r], gadd, ln) * m);
-          p.mx_scale[row * nb + blk] = static_cast<uint8_t>(c);
+          p.mx_scale[mx_row_scale_at(p, row, blk)] = static_cast<uint8_t>(c);
         }
       } else {
         for (int64_t idx = tid; idx < static_cast<int64_t>(nr) * H; idx += 256) {
@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(256) fwd_generic_kernel(const FwdParams p) {
           for (int r = 0; r < 32; ++r)
             p.colwise_out[(i0 + r) * H + j] =
                 e4m3(z_at<Tin>(p, i0 + r, j, s_mean[r], s_rs[r], gadd, ln) * m);
-          p.mx_colwise_scale[s * H + j] = static_cast<uint8_t>(c);
+          p.mx_colwise_scale[mx_col_scale_at(p, s, j)] = static_cast<uint8_t>(c);
         }
       }
     }

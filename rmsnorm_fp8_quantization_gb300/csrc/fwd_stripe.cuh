@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
         for (int e = 0; e < VEC; ++e) cm[e] = 0.f;
         uint8_t* orow = p.write_rowwise ? reinterpret_cast<uint8_t*>(p.out) + (i0 + rp) * H + col
                                         : nullptr;
-        uint8_t* srow = p.write_rowwise ? p.mx_scale + (i0 + rp) * sc_stride + col / 32 : nullptr;
+        int64_t srow = mx_row_scale_at(p, i0 + rp, col / 32);
 #pragma unroll 2
         for (int r = rp; r < kStripeRows; r += 2) {
           uint64_t z[NPV];
@@ -287,9 +287,9 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
 #pragma unroll
             for (int i = 0; i < VEC / 4; ++i) q[i] = e4m3x4_pairs(z[2 * i], z[2 * i + 1], s2);
             st_words<VEC / 4>(orow, q);
-            if ((v & (TPB - 1)) == 0) *srow = static_cast<uint8_t>(code);
+            if ((v & (TPB - 1)) == 0) p.mx_scale[srow] = static_cast<uint8_t>(code);
             orow += 2 * H;
-            srow += 2 * sc_stride;
+            srow = p.mx_swizzle ? mx_row_scale_at(p, i0 + r + 2, col / 32) : srow + 2 * sc_stride;
           }
         }
         if (p.write_colwise) {
@@ -309,7 +309,16 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
             gm[i] = mul2(gw[i], m01);
             bm[i] = mul2(bw[i], m01);
           }
-          if (rp == 0) st_words<VEC / 4>(p.mx_colwise_scale + stripe_of(k) * H + col, cw);
+          if (rp == 0) {
+            if (p.mx_swizzle) {
+#pragma unroll
+              for (int e = 0; e < VEC; ++e)
+                p.mx_colwise_scale[mx_col_scale_at(p, stripe_of(k), col + e)] =
+                    static_cast<uint8_t>(cw[e / 4] >> (8 * (e & 3)));
+            } else {
+              st_words<VEC / 4>(p.mx_colwise_scale + stripe_of(k) * H + col, cw);
+            }
+          }
           uint8_t* crow = p.colwise_out + (i0 + rp) * H + col;
 #pragma unroll 2
           for (int r = rp; r < kStripeRows; r += 2) {

@@ -336,6 +336,26 @@ __device__ __forceinline__ float e8m0_mult(uint32_t code) {
   return code == 255u ? __uint_as_float(0x7FFFFFFFu) : __uint_as_float((254u - code) << 23);
 }
 
+// Byte offset of scale (r, c) in the tiled GEMM order: 512-byte tiles of
+// 128 x 4 scales, `tiles_per_row` tiles (of 4 columns) per 128 rows, scale
+// (r, c) of a tile at 16 * (r % 32) + 4 * (r / 32) + c.
+__device__ __forceinline__ int64_t mx_tiled_offset(int64_t r, int64_t c, int64_t tiles_per_row) {
+  return ((r >> 7) * tiles_per_row + (c >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (c & 3);
+}
+// Index of the rowwise MXFP8 scale of (row, block) in p.mx_scale.
+__device__ __forceinline__ int64_t mx_row_scale_at(const FwdParams& p, int64_t row, int64_t blk) {
+  const int64_t nb = p.hidden / 32;
+  return p.mx_swizzle ? mx_tiled_offset(row, blk, (nb + 3) / 4) : row * nb + blk;
+}
+// Index of the columnwise MXFP8 scale of (32-row stripe, column) in
+// p.mx_colwise_scale; the tiled order treats the operand as transposed.
+__device__ __forceinline__ int64_t mx_col_scale_at(const FwdParams& p, int64_t stripe,
+                                                   int64_t col) {
+  const int64_t ns = p.rows / 32;
+  return p.mx_swizzle ? mx_tiled_offset(col, stripe, (ns + 3) / 4)
+                      : stripe * p.hidden + col;
+}
+
 // ---------------------------------------------------------------- reductions
 
 __device__ __forceinline__ float warp_sum(float v) {

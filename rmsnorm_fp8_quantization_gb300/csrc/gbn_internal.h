@@ -54,6 +54,7 @@ struct FwdParams {
   int w_dt;                  // weight dtype (Dt)
   int write_rowwise;
   int write_colwise;
+  int mx_swizzle;            // MXFP8 scales in the padded 128x4-tiled GEMM order
 };
 
 struct BwdParams {

@@ -263,7 +263,8 @@ __global__ void __launch_bounds__(fwd_ring_max_threads(NV)) fwd_ring_kernel(cons
           if constexpr (QM == Q_MXFP8) {
             constexpr int TPB = 32 / VEC;
             if ((tid & (TPB - 1)) == 0)
-              p.mx_scale[sched.row(k) * (H / 32) + (v * VEC) / 32] = static_cast<uint8_t>(code);
+              p.mx_scale[mx_row_scale_at(p, sched.row(k), (v * VEC) / 32)] =
+                  static_cast<uint8_t>(code);
           }
         }
       }

@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libgbnorm.so")
 GBN_LAYERNORM, GBN_RMSNORM = 0, 1
 GBN_SCALING_NONE, GBN_SCALING_DELAYED_TENSOR, GBN_SCALING_MXFP8_1D = 0, 1, 2
 GBN_LAYOUT_ROWWISE, GBN_LAYOUT_COLWISE, GBN_LAYOUT_ROWWISE_COLWISE = 0, 1, 2
+GBN_LAYOUT_SWIZZLED_SCALES = 0x100  # OR-ed into the layout (MXFP8)
 GBN_F32, GBN_BF16, GBN_F16, GBN_E4M3, GBN_E8M0 = 0, 1, 2, 3, 4
 (GBN_OK, GBN_ERR_NULL, GBN_ERR_DTYPE, GBN_ERR_SHAPE, GBN_ERR_ALIGNMENT, GBN_ERR_WORKSPACE,
  GBN_ERR_ENUM, GBN_ERR_CUDA) = range(8)

@@ -22,8 +22,22 @@ def _check(st, where):
         raise G.GbnError(st, where)
 
 
+def _roundup(a, b):
+    return (a + b - 1) // b * b
+
+
+def mx_scale_shapes(rows, hidden, swizzled=False):
+    """Shapes of the MXFP8 (rowwise, colwise) E8M0 scale buffers.  Swizzled:
+    padded to the 128 x 4 tiles of the GEMM order (colwise as the transposed
+    operand: hidden outer, rows/32 inner)."""
+    if not swizzled:
+        return (rows, hidden // 32), (rows // 32, hidden)
+    return ((_roundup(rows, 128), _roundup(hidden // 32, 4)),
+            (_roundup(hidden, 128), _roundup(rows // 32, 4)))
+
+
 def fwd_outputs(rows, hidden, in_dtype, norm="layernorm", scaling="none", layout="rowwise",
-                device="cuda", training=True):
+                device="cuda", training=True, swizzled_scales=False):
     """Allocates every output buffer the forward writes for this configuration."""
     dev = torch.device(device)
     o = {"out": None, "colwise_out": None, "mu": None, "rsigma": None, "scale_inv": None,
@@ -45,28 +59,32 @@ def fwd_outputs(rows, hidden, in_dtype, norm="layernorm", scaling="none", layout
             o["colwise_out"] = torch.empty(hidden, rows, dtype=torch.uint8, device=dev)
             o["colwise_scale_inv"] = torch.empty(1, dtype=torch.float32, device=dev)
     elif scaling == "mxfp8":
+        rs, cs = mx_scale_shapes(rows, hidden, swizzled_scales)
         if rowwise:
-            o["scale_inv"] = torch.empty(rows, hidden // 32, dtype=torch.uint8, device=dev)
+            o["scale_inv"] = torch.empty(rs, dtype=torch.uint8, device=dev)
         if colwise:
             o["colwise_out"] = torch.empty(rows, hidden, dtype=torch.uint8, device=dev)
-            o["colwise_scale_inv"] = torch.empty(rows // 32, hidden, dtype=torch.uint8,
-                                                 device=dev)
+            o["colwise_scale_inv"] = torch.empty(cs, dtype=torch.uint8, device=dev)
     return o
 
 
 def norm_fwd(x, gamma, beta=None, *, norm="layernorm", eps=1e-5, zero_centered_gamma=False,
              scaling="none", layout="rowwise", scale=None, amax=None, sm_margin=0,
-             training=True, outputs=None, stream=None):
-    """Runs the fused forward; returns the dict of output tensors."""
+             training=True, outputs=None, stream=None, swizzled_scales=False):
+    """Runs the fused forward; returns the dict of output tensors.
+    ``swizzled_scales`` (MXFP8): scales in the padded, tiled GEMM order."""
     rows, hidden = x.shape
     o = outputs if outputs is not None else fwd_outputs(rows, hidden, x.dtype, norm, scaling,
-                                                        layout, x.device, training)
+                                                        layout, x.device, training,
+                                                        swizzled_scales)
     in_dt = G.TORCH_DTYPE[x.dtype]
     out_dt = in_dt if scaling == "none" else G.GBN_E4M3
     st = G.gbn_norm_fwd(x, gamma, beta, scale, amax, o["out"], o["colwise_out"], o["mu"],
                         o["rsigma"], o["scale_inv"], o["colwise_scale_inv"], o["updated_amax"],
                         None, 0, rows, hidden, in_dt, G.TORCH_DTYPE[gamma.dtype], out_dt,
-                        _NORM[norm], _SCALING[scaling], _LAYOUT[layout], zero_centered_gamma,
+                        _NORM[norm], _SCALING[scaling],
+                        _LAYOUT[layout] | (G.GBN_LAYOUT_SWIZZLED_SCALES if swizzled_scales else 0),
+                        zero_centered_gamma,
                         eps, sm_margin, stream)
     _check(st, "gbn_norm_fwd")
     return o

@@ -34,8 +34,8 @@ def test_header_functions_are_exported(G):
 
 def test_header_enums_match_binding(G):
     text = open(os.path.join(ROOT, "include", "gbnorm.h")).read()
-    for name, val in re.findall(r"\b(GBN_[A-Z0-9_]+)\s*=\s*(\d+)", text):
-        assert getattr(G, name) == int(val), name
+    for name, val in re.findall(r"\b(GBN_[A-Z0-9_]+)\s*=\s*(0x[0-9a-fA-F]+|\d+)", text):
+        assert getattr(G, name) == int(val, 0), name
 
 
 def test_status_strings(G):

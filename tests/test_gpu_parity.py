@@ -135,6 +135,13 @@ FWD_DELAYED_CASES = [
     wl(DEL, rows=32, hidden=24, in_dtype="f32", w_dtype="f32"),
     wl(DEL, rows=40, hidden=36, in_dtype="f16"),            # hidden % 8 != 0: generic
     wl(DEL, rows=64, hidden=12288, amax_prev=4.0),          # heavy saturation
+    # LayerNorm in every layout
+    wl(DEL, rows=96, hidden=4096, norm="layernorm", w_dtype="f32", beta_std=0.1,
+       layout="colwise"),
+    wl(DEL, rows=67, hidden=4000, norm="layernorm", w_dtype="f32", beta_std=0.1,
+       layout="rowwise"),
+    wl(DEL, rows=64, hidden=8192, norm="layernorm", w_dtype="bf16", beta_std=0.1,
+       zero_centered_gamma=True, gamma_mean=0.0, gamma_std=0.05),
 ]
 
 
@@ -153,6 +160,14 @@ FWD_MX_CASES = [
     wl(MX, rows=64, hidden=2048, in_dtype="f16", zero_centered_gamma=False, gamma_mean=1.0,
        gamma_std=0.1),
     wl(MX, rows=40, hidden=96, layout="rowwise"),           # rowwise allows ragged rows
+    # LayerNorm in every layout
+    wl(MX, rows=96, hidden=5120, norm="layernorm", w_dtype="f32", beta_std=0.1,
+       zero_centered_gamma=False, gamma_mean=1.0, gamma_std=0.1),
+    wl(MX, rows=64, hidden=8192, norm="layernorm", w_dtype="bf16", beta_std=0.1),
+    wl(MX, rows=64, hidden=2048, norm="layernorm", w_dtype="f32", beta_std=0.1,
+       layout="colwise"),
+    wl(MX, rows=77, hidden=4096, norm="layernorm", w_dtype="f32", beta_std=0.1,
+       layout="rowwise", in_dtype="f16"),
 ]
 
 

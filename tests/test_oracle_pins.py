@@ -433,3 +433,34 @@ def test_bwd_zero_centered_gamma_uses_one_plus_gamma(orc):
     b, gb, _ = orc.norm_bwd(dz, x, None, rs32, gamma + 1, None, RMS, False)  # exact on grid
     np.testing.assert_allclose(a, b, rtol=1e-15, atol=1e-15)
     np.testing.assert_allclose(ga, gb, rtol=1e-15, atol=1e-15)
+
+
+# ---------------------------------------------------------------- GEMM-ready scale order
+
+def test_mxfp8_swizzle_golden_offsets(orc):
+    """Offsets worked by hand from the tile description (tests/golden)."""
+    R, B = 130, 5
+    s = (np.arange(R * B, dtype=np.int64).reshape(R, B) * 7 % 251 + 1).astype(np.uint8)
+    out, held = orc.mxfp8_swizzle(s)
+    assert out.size == 256 * 8 and held.sum() == R * B
+    for r, c, off in read_golden("mxfp8_swizzle.txt"):
+        r, c, off = int(r), int(c), int(off)
+        assert held[off] and out[off] == s[r, c], (r, c, off)
+
+
+def test_mxfp8_swizzle_is_a_padded_permutation(orc):
+    g = np.random.default_rng(3)
+    for R, B in [(128, 4), (1, 1), (300, 9), (256, 160)]:
+        s = g.integers(1, 255, size=(R, B)).astype(np.uint8)
+        out, held = orc.mxfp8_swizzle(s)
+        Rp, Bp = -(-R // 128) * 128, -(-B // 4) * 4
+        assert out.size == Rp * Bp
+        assert held.sum() == R * B and np.all(out[~held] == 0)
+        assert sorted(out[held].tolist()) == sorted(s.ravel().tolist())
+        # an exactly tiled matrix: every 512-byte tile holds one 128 x 4 block
+        if R % 128 == 0 and B % 4 == 0:
+            tiles = out.reshape(R // 128, B // 4, 512)
+            for tr in range(R // 128):
+                for tc in range(B // 4):
+                    blk = s[tr * 128:(tr + 1) * 128, tc * 4:(tc + 1) * 4]
+                    assert sorted(tiles[tr, tc].tolist()) == sorted(blk.ravel().tolist())
