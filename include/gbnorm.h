@@ -227,6 +227,42 @@ gbn_status gbn_norm_bwd_noalloc(const void* dz, const void* x, const float* mu,
 #define GBN_DEVICE_ERR_COPY_TIMEOUT 1u
 gbn_status gbn_device_error(unsigned int* flags, int clear);
 
+/* ---- Scaled (masked) softmax ("Migrate norms and softmax kernels to NVRTC",
+ * Description and JIT cost table: scaled_masked_softmax,
+ * scaled_upper_triang_masked_softmax, scaled_aligned_causal_masked_softmax,
+ * forward and backward).  The page gives no formulas; the plain definitions
+ * are used:
+ *   y  = softmax over the last axis of scale * x, over the kept positions;
+ *        masked positions get 0, and a row with no kept position is all 0;
+ *   dx = scale * y * (dy - sum_j dy * y)   (y: the forward's output). */
+typedef enum {
+  GBN_SOFTMAX_NO_MASK = 0,
+  GBN_SOFTMAX_PADDING = 1,        /* mask [mask_batches, 1, sq, sk] u8, nonzero = masked;
+                                     batch b uses mask batch b % mask_batches */
+  GBN_SOFTMAX_CAUSAL_UPPER = 2,   /* sq == sk; (i, j) kept iff j <= i */
+  GBN_SOFTMAX_CAUSAL_ALIGNED = 3  /* bottom-right aligned; kept iff j <= i + (sk - sq) */
+} gbn_softmax_mask;
+
+/* Longest row (keys) of the softmax.  Rows whose byte length is not a
+ * multiple of 16, or whose pointers are not 16-byte aligned, take a scalar
+ * path limited to 2048 keys (longer: GBN_ERR_SHAPE). */
+#define GBN_SOFTMAX_MAX_KEYS 16384
+
+/* Forward.  x, y: [batches, heads, sq, sk] row-major in dtype (F32, BF16 or
+ * F16), y may alias x; mask: see gbn_softmax_mask, NULL unless PADDING.
+ * fp32 arithmetic.  Returns GBN_ERR_SHAPE for sk outside [1,
+ * GBN_SOFTMAX_MAX_KEYS] or sq != sk with CAUSAL_UPPER; no rows: GBN_OK with
+ * nothing enqueued. */
+gbn_status gbn_softmax_fwd(const void* x, const uint8_t* mask, void* y, int64_t batches,
+                           int64_t heads, int64_t sq, int64_t sk, int64_t mask_batches,
+                           gbn_dtype dtype, gbn_softmax_mask mask_kind, float scale,
+                           cudaStream_t stream);
+
+/* Backward over `rows` rows of sk: dy, y, dx in dtype; dx may alias dy.
+ * Masked positions have y = 0 and so dx = 0: no mask argument. */
+gbn_status gbn_softmax_bwd(const void* dy, const void* y, void* dx, int64_t rows, int64_t sk,
+                           gbn_dtype dtype, float scale, cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* gbn_status_string(gbn_status status);
 

@@ -19,7 +19,7 @@ LIB = os.path.join(PKG, "libgbnorm.so")
 BUILD_DIR = os.path.join(PKG, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["api.cu", "kernels_f32.cu", "kernels_bf16.cu", "kernels_f16.cu", "finalize.cu",
-           "noalloc.cu"]
+           "noalloc.cu", "softmax.cu"]
 
 
 def _nvcc() -> str:

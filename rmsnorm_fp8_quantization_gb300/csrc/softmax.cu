@@ -1,0 +1,349 @@
+// Scaled (masked) softmax, forward and backward: the softmax kernels named
+// on "Migrate norms and softmax kernels to NVRTC" (Description:
+// scaled_masked_softmax, scaled_upper_triang_masked_softmax,
+// scaled_aligned_causal_masked_softmax; forward and backward).  The page
+// gives no formulas; these follow the plain definitions:
+//   y  = softmax over the last axis of scale * x, over the kept positions
+//        (masked ones are 0; a row with nothing kept is all 0);
+//   dx = scale * y * (dy - sum_j dy * y).
+//
+// A row of sk elements is handled by a group of G = 32 * WPR threads (WPR
+// warps, one to eight), each holding NV loads of V elements in registers, so a
+// row is read once and written once.  The reductions (max, then sum; or
+// sum dy * y) run over the group: warp shuffles, then shared memory when
+// WPR > 1.  exp is taken as exp2f of x * scale * log2(e) less its row
+// maximum.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "gbnorm.h"
+#include "gbn_device.cuh"
+
+namespace gbn {
+namespace {
+
+constexpr int kSmThreads = 256;
+constexpr int64_t kMaxSoftmaxKeys = GBN_SOFTMAX_MAX_KEYS;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <typename T>
+struct SmElem;
+template <>
+struct SmElem<float> {
+  static __device__ float get(const float* p) { return *p; }
+  static __device__ void put(float* p, float v) { *p = v; }
+};
+template <>
+struct SmElem<__nv_bfloat16> {
+  static __device__ float get(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+  static __device__ void put(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+};
+template <>
+struct SmElem<__half> {
+  static __device__ float get(const __half* p) { return __half2float(*p); }
+  static __device__ void put(__half* p, float v) { *p = __float2half_rn(v); }
+};
+
+// Loads V consecutive elements (16 bytes when V = 16 / sizeof(T)) as floats.
+template <typename T, int V>
+__device__ __forceinline__ void load_v(const T* p, float* f) {
+  if constexpr (V == 1) {
+    f[0] = SmElem<T>::get(p);
+  } else {
+    const uint4 u = ld_stream16(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    uint64_t pr[V / 2];
+    widen_pairs<T, V>(w, pr);
+#pragma unroll
+    for (int i = 0; i < V / 2; ++i) {
+      const float2 t = u2(pr[i]);
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  }
+}
+template <typename T, int V>
+__device__ __forceinline__ void store_v(T* p, const float* f) {
+  if constexpr (V == 1) {
+    SmElem<T>::put(p, f[0]);
+  } else {
+    uint64_t pr[V / 2];
+#pragma unroll
+    for (int i = 0; i < V / 2; ++i) pr[i] = p2(f[2 * i], f[2 * i + 1]);
+    uint32_t w[Words<T, V>::n];
+    narrow_pairs<T, V>(pr, w);
+    st_words<Words<T, V>::n>(p, w);
+  }
+}
+
+// Group-wide reduction (max or sum) over the WPR warps of one row.  `buf`:
+// kSmThreads / 32 floats; all rows of the CTA call it together.
+template <bool MAX>
+__device__ __forceinline__ float group_reduce(float v, float* buf, int wpr) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float u = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    v = MAX ? fmaxf(v, u) : v + u;
+  }
+  if (wpr == 1) return v;
+  const int warp = threadIdx.x >> 5, first = warp - warp % wpr;
+  if ((threadIdx.x & 31) == 0) buf[warp] = v;
+  __syncthreads();
+  float r = buf[first];
+  for (int w = 1; w < wpr; ++w) r = MAX ? fmaxf(r, buf[first + w]) : r + buf[first + w];
+  __syncthreads();
+  return r;
+}
+
+struct SmFwdParams {
+  const void* x;
+  const uint8_t* mask;
+  void* y;
+  int64_t rows;        // batches * heads * sq
+  int64_t heads_sq;    // heads * sq
+  int64_t sq;
+  int64_t mask_batches;
+  int sk;
+  int wpr;             // warps per row
+  float scale_log2e;
+};
+
+// Forward.  MASK: 0 none, 1 padding mask, 2 upper-triangular, 3 aligned causal.
+template <typename T, int V, int NV, int MASK>
+__global__ void __launch_bounds__(kSmThreads) softmax_fwd_kernel(const SmFwdParams p) {
+  pdl_begin();
+  __shared__ float buf[kSmThreads / 32];
+  const int gthreads = 32 * p.wpr;
+  const int rows_per_cta = kSmThreads / gthreads;
+  const int g = threadIdx.x / gthreads, t = threadIdx.x % gthreads;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * rows_per_cta + g;
+  const bool live = row < p.rows;
+  const int sk = p.sk;
+  const int64_t rr = live ? row : 0;
+  const int64_t i = rr % p.sq;  // query index
+  int limit = sk;               // causal: positions j < limit are kept
+  if constexpr (MASK == 2) limit = static_cast<int>(i) + 1;
+  if constexpr (MASK == 3) {
+    const int64_t l = i + 1 + (sk - p.sq);
+    limit = l < 0 ? 0 : (l > sk ? sk : static_cast<int>(l));
+  }
+  const T* xr = reinterpret_cast<const T*>(p.x) + rr * sk;
+  const uint8_t* mr = nullptr;
+  if constexpr (MASK == 1)
+    mr = p.mask + ((rr / p.heads_sq) % p.mask_batches * p.sq + i) * static_cast<int64_t>(sk);
+
+  float u[NV][V];
+  float m = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int j0 = (k * gthreads + t) * V;
+    if (live && j0 < sk) {
+      load_v<T, V>(xr + j0, u[k]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < V; ++e) u[k][e] = 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < V; ++e) {
+      const int j = j0 + e;
+      bool keep = live && j < limit;
+      if constexpr (MASK == 1) keep = keep && mr[j] == 0;
+      u[k][e] = keep ? u[k][e] * p.scale_log2e : -INFINITY;
+      m = fmaxf(m, u[k][e]);
+    }
+  }
+  m = group_reduce<true>(m, buf, p.wpr);
+  const float mo = m == -INFINITY ? 0.f : m;  // nothing kept: every term is exp2(-inf) = 0
+  float s = 0.f;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+#pragma unroll
+    for (int e = 0; e < V; ++e) {
+      u[k][e] = exp2f(u[k][e] - mo);
+      s += u[k][e];
+    }
+  }
+  s = group_reduce<false>(s, buf, p.wpr);
+  const float inv = s > 0.f ? 1.f / s : 0.f;
+  T* yr = reinterpret_cast<T*>(p.y) + rr * sk;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int j0 = (k * gthreads + t) * V;
+    if (live && j0 < sk) {
+#pragma unroll
+      for (int e = 0; e < V; ++e) u[k][e] *= inv;
+      store_v<T, V>(yr + j0, u[k]);
+    }
+  }
+}
+
+struct SmBwdParams {
+  const void* dy;
+  const void* y;
+  void* dx;
+  int64_t rows;
+  int sk;
+  int wpr;
+  float scale;
+};
+
+template <typename T, int V, int NV>
+__global__ void __launch_bounds__(kSmThreads) softmax_bwd_kernel(const SmBwdParams p) {
+  pdl_begin();
+  __shared__ float buf[kSmThreads / 32];
+  const int gthreads = 32 * p.wpr;
+  const int rows_per_cta = kSmThreads / gthreads;
+  const int g = threadIdx.x / gthreads, t = threadIdx.x % gthreads;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * rows_per_cta + g;
+  const bool live = row < p.rows;
+  const int sk = p.sk;
+  const int64_t rr = live ? row : 0;
+  const T* yr = reinterpret_cast<const T*>(p.y) + rr * sk;
+  const T* dr = reinterpret_cast<const T*>(p.dy) + rr * sk;
+  float yv[NV][V], dv[NV][V];
+  float c = 0.f;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int j0 = (k * gthreads + t) * V;
+    if (live && j0 < sk) {
+      load_v<T, V>(yr + j0, yv[k]);
+      load_v<T, V>(dr + j0, dv[k]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < V; ++e) yv[k][e] = dv[k][e] = 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < V; ++e) c = fmaf(yv[k][e], dv[k][e], c);
+  }
+  c = group_reduce<false>(c, buf, p.wpr);
+  T* xr = reinterpret_cast<T*>(p.dx) + rr * sk;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int j0 = (k * gthreads + t) * V;
+    if (live && j0 < sk) {
+      float o[V];
+#pragma unroll
+      for (int e = 0; e < V; ++e) o[e] = p.scale * yv[k][e] * (dv[k][e] - c);
+      store_v<T, V>(xr + j0, o);
+    }
+  }
+}
+
+// ---- host side
+
+// Loads per thread (NV) and warps per row (WPR) for a row of sk elements in
+// loads of V: the smallest WPR (1..8) with NV <= 8, then the smallest NV.
+bool sm_geom(int sk, int v, int* nv, int* wpr) {
+  for (int w = 1; w <= kSmThreads / 32; w *= 2) {
+    for (int n = 1; n <= 8; n *= 2) {
+      if (static_cast<int64_t>(32) * w * n * v >= sk) {
+        *nv = n;
+        *wpr = w;
+        return true;
+      }
+    }
+  }
+  return false;
+}
+
+template <typename T, int V, int NV>
+cudaError_t launch_fwd_nv(const SmFwdParams& p, int mask, int grid, cudaStream_t st) {
+  switch (mask) {
+    case 0: return launch_pdl(softmax_fwd_kernel<T, V, NV, 0>, dim3(grid), dim3(kSmThreads), 0, st, p);
+    case 1: return launch_pdl(softmax_fwd_kernel<T, V, NV, 1>, dim3(grid), dim3(kSmThreads), 0, st, p);
+    case 2: return launch_pdl(softmax_fwd_kernel<T, V, NV, 2>, dim3(grid), dim3(kSmThreads), 0, st, p);
+    default: return launch_pdl(softmax_fwd_kernel<T, V, NV, 3>, dim3(grid), dim3(kSmThreads), 0, st, p);
+  }
+}
+
+template <typename T, int V>
+cudaError_t launch_fwd(const SmFwdParams& p, int mask, int nv, int grid, cudaStream_t st) {
+  switch (nv) {
+    case 1: return launch_fwd_nv<T, V, 1>(p, mask, grid, st);
+    case 2: return launch_fwd_nv<T, V, 2>(p, mask, grid, st);
+    case 4: return launch_fwd_nv<T, V, 4>(p, mask, grid, st);
+    default: return launch_fwd_nv<T, V, 8>(p, mask, grid, st);
+  }
+}
+
+template <typename T, int V>
+cudaError_t launch_bwd(const SmBwdParams& p, int nv, int grid, cudaStream_t st) {
+  const dim3 g(grid), b(kSmThreads);
+  switch (nv) {
+    case 1: return launch_pdl(softmax_bwd_kernel<T, V, 1>, g, b, 0, st, p);
+    case 2: return launch_pdl(softmax_bwd_kernel<T, V, 2>, g, b, 0, st, p);
+    case 4: return launch_pdl(softmax_bwd_kernel<T, V, 4>, g, b, 0, st, p);
+    default: return launch_pdl(softmax_bwd_kernel<T, V, 8>, g, b, 0, st, p);
+  }
+}
+
+int sm_esize(gbn_dtype d) { return d == GBN_F32 ? 4 : 2; }
+bool sm_aligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace gbn
+
+using namespace gbn;
+
+extern "C" {
+
+gbn_status gbn_softmax_fwd(const void* x, const uint8_t* mask, void* y, int64_t batches,
+                           int64_t heads, int64_t sq, int64_t sk, int64_t mask_batches,
+                           gbn_dtype dtype, gbn_softmax_mask mask_kind, float scale,
+                           cudaStream_t stream) {
+  if (dtype != GBN_F32 && dtype != GBN_BF16 && dtype != GBN_F16) return GBN_ERR_DTYPE;
+  if (mask_kind < GBN_SOFTMAX_NO_MASK || mask_kind > GBN_SOFTMAX_CAUSAL_ALIGNED) return GBN_ERR_ENUM;
+  if (batches < 0 || heads < 0 || sq < 0 || sk < 1 || sk > kMaxSoftmaxKeys) return GBN_ERR_SHAPE;
+  if (mask_kind == GBN_SOFTMAX_CAUSAL_UPPER && sq != sk) return GBN_ERR_SHAPE;
+  const int64_t rows = batches * heads * sq;
+  if (rows == 0) return GBN_OK;
+  if (!x || !y) return GBN_ERR_NULL;
+  if (mask_kind == GBN_SOFTMAX_PADDING && (!mask || mask_batches < 1)) return GBN_ERR_NULL;
+  const int vec = 16 / sm_esize(dtype);
+  const bool vok = sk % vec == 0 && sm_aligned(x) && sm_aligned(y);
+  int nv = 0, wpr = 0;
+  if (!sm_geom(static_cast<int>(sk), vok ? vec : 1, &nv, &wpr)) return GBN_ERR_SHAPE;
+  SmFwdParams p{x, mask, y, rows, heads * sq, sq, mask_batches, static_cast<int>(sk), wpr,
+                scale * kLog2e};
+  const int64_t rows_per_cta = kSmThreads / (32 * wpr);
+  const int64_t grid = (rows + rows_per_cta - 1) / rows_per_cta;
+  if (grid > 0x7FFFFFFF) return GBN_ERR_SHAPE;
+  const int m = static_cast<int>(mask_kind), g = static_cast<int>(grid);
+  cudaError_t e;
+  if (dtype == GBN_F32)
+    e = vok ? launch_fwd<float, 4>(p, m, nv, g, stream) : launch_fwd<float, 1>(p, m, nv, g, stream);
+  else if (dtype == GBN_BF16)
+    e = vok ? launch_fwd<__nv_bfloat16, 8>(p, m, nv, g, stream)
+            : launch_fwd<__nv_bfloat16, 1>(p, m, nv, g, stream);
+  else
+    e = vok ? launch_fwd<__half, 8>(p, m, nv, g, stream) : launch_fwd<__half, 1>(p, m, nv, g, stream);
+  return e == cudaSuccess ? GBN_OK : GBN_ERR_CUDA;
+}
+
+gbn_status gbn_softmax_bwd(const void* dy, const void* y, void* dx, int64_t rows, int64_t sk,
+                           gbn_dtype dtype, float scale, cudaStream_t stream) {
+  if (dtype != GBN_F32 && dtype != GBN_BF16 && dtype != GBN_F16) return GBN_ERR_DTYPE;
+  if (rows < 0 || sk < 1 || sk > kMaxSoftmaxKeys) return GBN_ERR_SHAPE;
+  if (rows == 0) return GBN_OK;
+  if (!dy || !y || !dx) return GBN_ERR_NULL;
+  const int vec = 16 / sm_esize(dtype);
+  const bool vok = sk % vec == 0 && sm_aligned(dy) && sm_aligned(y) && sm_aligned(dx);
+  int nv = 0, wpr = 0;
+  if (!sm_geom(static_cast<int>(sk), vok ? vec : 1, &nv, &wpr)) return GBN_ERR_SHAPE;
+  SmBwdParams p{dy, y, dx, rows, static_cast<int>(sk), wpr, scale};
+  const int64_t rows_per_cta = kSmThreads / (32 * wpr);
+  const int64_t grid = (rows + rows_per_cta - 1) / rows_per_cta;
+  if (grid > 0x7FFFFFFF) return GBN_ERR_SHAPE;
+  const int g = static_cast<int>(grid);
+  cudaError_t e;
+  if (dtype == GBN_F32)
+    e = vok ? launch_bwd<float, 4>(p, nv, g, stream) : launch_bwd<float, 1>(p, nv, g, stream);
+  else if (dtype == GBN_BF16)
+    e = vok ? launch_bwd<__nv_bfloat16, 8>(p, nv, g, stream)
+            : launch_bwd<__nv_bfloat16, 1>(p, nv, g, stream);
+  else
+    e = vok ? launch_bwd<__half, 8>(p, nv, g, stream) : launch_bwd<__half, 1>(p, nv, g, stream);
+  return e == cudaSuccess ? GBN_OK : GBN_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -28,7 +28,11 @@ GBN_F32, GBN_BF16, GBN_F16, GBN_E4M3, GBN_E8M0 = 0, 1, 2, 3, 4
 TORCH_DTYPE = {torch.float32: GBN_F32, torch.bfloat16: GBN_BF16, torch.float16: GBN_F16}
 
 FUNCTIONS = ("gbn_norm_fwd_workspace_size", "gbn_norm_fwd", "gbn_norm_bwd_workspace_size",
-             "gbn_norm_bwd", "gbn_norm_bwd_noalloc", "gbn_device_error", "gbn_status_string")
+             "gbn_norm_bwd", "gbn_norm_bwd_noalloc", "gbn_device_error", "gbn_status_string",
+             "gbn_softmax_fwd", "gbn_softmax_bwd")
+(GBN_SOFTMAX_NO_MASK, GBN_SOFTMAX_PADDING, GBN_SOFTMAX_CAUSAL_UPPER,
+ GBN_SOFTMAX_CAUSAL_ALIGNED) = range(4)
+GBN_SOFTMAX_MAX_KEYS = 16384
 GBN_DEVICE_ERR_COPY_TIMEOUT = 1
 
 
@@ -60,6 +64,10 @@ def _load():
     lib.gbn_norm_bwd_noalloc.restype = I
     lib.gbn_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), I]
     lib.gbn_device_error.restype = I
+    lib.gbn_softmax_fwd.argtypes = [P, P, P, I64, I64, I64, I64, I64, I, I, F, P]
+    lib.gbn_softmax_fwd.restype = I
+    lib.gbn_softmax_bwd.argtypes = [P, P, P, I64, I64, I, F, P]
+    lib.gbn_softmax_bwd.restype = I
     lib.gbn_status_string.argtypes = [I]
     lib.gbn_status_string.restype = ctypes.c_char_p
     return lib
@@ -153,3 +161,14 @@ def gbn_norm_bwd_noalloc(dz, x, mu, rsigma, gamma, dresidual, dx, dgamma, dbeta,
                                      _ptr(dresidual), _ptr(dx), _ptr(dgamma), _ptr(dbeta), rows,
                                      hidden, in_dtype, w_dtype, norm_type,
                                      int(bool(zero_centered_gamma)), sm_margin, _stream(stream))
+
+
+def gbn_softmax_fwd(x, mask, y, batches, heads, sq, sk, mask_batches, dtype, mask_kind, scale,
+                    stream=None) -> int:
+    return _lib.gbn_softmax_fwd(_ptr(x), _ptr(mask), _ptr(y), batches, heads, sq, sk,
+                                mask_batches, dtype, mask_kind, float(scale), _stream(stream))
+
+
+def gbn_softmax_bwd(dy, y, dx, rows, sk, dtype, scale, stream=None) -> int:
+    return _lib.gbn_softmax_bwd(_ptr(dy), _ptr(y), _ptr(dx), rows, sk, dtype, float(scale),
+                                _stream(stream))

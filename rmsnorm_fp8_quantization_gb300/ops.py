@@ -118,3 +118,29 @@ def norm_bwd(dz, x, mu, rsigma, gamma, dresidual=None, *, norm="layernorm",
                         stream)
     _check(st, "gbn_norm_bwd")
     return dx, dgamma, dbeta if norm == "layernorm" else None
+
+
+_SOFTMAX_MASK = {"none": G.GBN_SOFTMAX_NO_MASK, "padding": G.GBN_SOFTMAX_PADDING,
+                 "causal": G.GBN_SOFTMAX_CAUSAL_UPPER,
+                 "causal_aligned": G.GBN_SOFTMAX_CAUSAL_ALIGNED}
+
+
+def softmax_fwd(x, scale=1.0, mask_kind="none", mask=None, out=None, stream=None):
+    """Scaled (masked) softmax over the last axis of x [batches, heads, sq, sk];
+    mask [mask_batches, 1, sq, sk] uint8 (nonzero = masked) for "padding"."""
+    b, h, sq, sk = x.shape
+    y = torch.empty_like(x) if out is None else out
+    mb = 0 if mask is None else mask.shape[0]
+    st = G.gbn_softmax_fwd(x, mask, y, b, h, sq, sk, mb, G.TORCH_DTYPE[x.dtype],
+                           _SOFTMAX_MASK[mask_kind], scale, stream)
+    _check(st, "gbn_softmax_fwd")
+    return y
+
+
+def softmax_bwd(dy, y, scale=1.0, out=None, stream=None):
+    """dx = scale * y * (dy - sum(dy * y)) over the last axis."""
+    sk = y.shape[-1]
+    dx = torch.empty_like(dy) if out is None else out
+    st = G.gbn_softmax_bwd(dy, y, dx, y.numel() // sk, sk, G.TORCH_DTYPE[y.dtype], scale, stream)
+    _check(st, "gbn_softmax_bwd")
+    return dx

@@ -125,3 +125,51 @@ def make_inputs(w: Workload, seed: int = 0, device: str = "cpu") -> dict:
         out["scale"] = torch.tensor([448.0 / w.amax_prev], dtype=torch.float32, device=device)
         out["amax"] = torch.tensor([w.amax_prev], dtype=torch.float32, device=device)
     return out
+
+
+# ---------------------------------------------------------------- softmax
+
+@dataclasses.dataclass(frozen=True)
+class SoftmaxWorkload:
+    name: str
+    batches: int
+    heads: int
+    sq: int
+    sk: int
+    dtype: str                 # "f32" | "bf16" | "f16"
+    mask: str = "none"         # "none" | "padding" | "causal" | "causal_aligned"
+    scale: float = 0.125
+    x_std: float = 4.0         # logits ~ x_std * N(0, 1)
+    mask_batches: int = 1
+    mask_frac: float = 0.25    # padding: fraction of masked positions
+
+    def with_shape(self, batches, heads, sq, sk) -> "SoftmaxWorkload":
+        return dataclasses.replace(self, batches=batches, heads=heads, sq=sq, sk=sk)
+
+
+SOFTMAX_WORKLOADS = {
+    # Causal (upper-triangular) attention probabilities, bf16, 8 x 16 heads x 2048 x 2048.
+    "softmax_causal_bf16_8x16x2048x2048": SoftmaxWorkload(
+        "softmax_causal_bf16_8x16x2048x2048", 8, 16, 2048, 2048, "bf16", mask="causal"),
+    # Padding-masked attention probabilities, bf16, 8 x 16 x 1024 x 1024, one mask per batch.
+    "softmax_padding_bf16_8x16x1024x1024": SoftmaxWorkload(
+        "softmax_padding_bf16_8x16x1024x1024", 8, 16, 1024, 1024, "bf16", mask="padding",
+        mask_batches=8),
+}
+
+
+def make_softmax_inputs(w: SoftmaxWorkload, seed: int = 0, device: str = "cpu") -> dict:
+    """Seeded inputs of a softmax workload: x (logits), dy, and the padding
+    mask (uint8, nonzero = masked) or None.  Draw order: x, dy, mask."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    shape = (w.batches, w.heads, w.sq, w.sk)
+    x = torch.empty(shape, dtype=torch.float32, device=device).normal_(generator=g)
+    x.mul_(w.x_std)
+    dy = torch.empty(shape, dtype=torch.float32, device=device).normal_(generator=g)
+    mask = None
+    if w.mask == "padding":
+        u = torch.rand((w.mask_batches, 1, w.sq, w.sk), generator=g, device=device)
+        mask = (u < w.mask_frac).to(torch.uint8)
+    dt = _DT[w.dtype]
+    return {"x": x.to(dt), "dy": dy.to(dt), "mask": mask}
