@@ -72,10 +72,11 @@ def bwd_bytes(w) -> int:
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """Samples SM clocks and throttle reasons with nvidia-smi every 50 ms.
-    `window()` marks the span whose samples count: it wraps the timed steps
-    plus a short stretch of the same steps on either side (the timed region
-    alone is a few milliseconds, shorter than the sampling period)."""
+    """Samples SM clocks and throttle reasons with nvidia-smi every 50 ms
+    while started.  The benchmark samples over the same back-to-back steps
+    just before and just after the timed steps, not during them: nvidia-smi
+    polling during the timed steps was measured to slow them (about 8 % per
+    step in three of four runs)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -83,47 +84,38 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.lines = []  # (monotonic time, csv line)
-        self.span = None
+        self.lines = []
 
-    def __enter__(self):
+    def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
-            self.thread.start()
-            t0 = time.monotonic()
-            while not self.lines and time.monotonic() - t0 < 10.0:
+            threading.Thread(target=self._read, args=(self.proc,), daemon=True).start()
+            n0, t0 = len(self.lines), time.monotonic()
+            while len(self.lines) == n0 and time.monotonic() - t0 < 10.0:
                 time.sleep(0.01)
         except (OSError, FileNotFoundError):
             self.proc = None
-        return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append((time.monotonic(), line.strip()))
+    def _read(self, proc):
+        for line in proc.stdout:
+            self.lines.append(line.strip())
 
-    def __exit__(self, *a):
+    def stop(self):
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-
-    def mark(self, start: bool):
-        t = time.monotonic()
-        self.span = (t, None) if start else (self.span[0], t)
+            self.proc = None
 
     def summary(self):
-        lo, hi = self.span if self.span and self.span[1] else (0.0, float("inf"))
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for t, ln in self.lines:
-            if not lo <= t <= hi:
-                continue
+        for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -139,7 +131,8 @@ class ClockSampler:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
                 "reasons": sorted(reasons), "samples": len(sm),
-                "window": "timed steps plus 0.3 s of the same steps before and after"}
+                "window": "0.5 s of the same back-to-back steps just before and just after "
+                          "the timed steps"}
 
 
 def run_for(calls, seconds):
@@ -309,12 +302,13 @@ def run_gpu(args):
     inp = make_inputs(w, seed=rank, device=str(dev))
     fwd, bwd, outs, grads = make_step(ops, w, inp)
     sampler = ClockSampler(dev.index)
-    with sampler:
-        sampler.mark(True)
-        run_for([fwd, bwd], 0.3)
-        per, tot = time_calls([fwd, bwd], args.steps, args.warmup, None, barrier)
-        run_for([fwd, bwd], 0.3)
-        sampler.mark(False)
+    sampler.start()
+    run_for([fwd, bwd], 0.5)
+    sampler.stop()
+    per, tot = time_calls([fwd, bwd], args.steps, args.warmup, None, barrier)
+    sampler.start()
+    run_for([fwd, bwd], 0.5)
+    sampler.stop()
     clocks = sampler.summary()
     ms_step = tot / args.steps
     if dist:
@@ -342,6 +336,7 @@ def run_gpu(args):
         del inp, outs, grads
         torch.cuda.empty_cache()
         detail = run_detail(ops, WORKLOADS, make_inputs, args, flush, dev, peak)
+        detail.update(run_softmax_detail(ops, args, flush, dev, peak))
 
     result = {
         "metric": METRIC,
@@ -462,6 +457,57 @@ def run_detail(ops, WORKLOADS, make_inputs, args, flush, dev, peak):
                       "fits_in_l2": nb < L2_BYTES}
         out[name] = d
         del inp, outs, grads, fwd, bwd
+        torch.cuda.empty_cache()
+    return out
+
+
+def softmax_bytes(w, pass_):
+    """Forward: the kept logits read (causal rows need none past their last
+    kept key), the mask read once, y written; backward: y, dy read, dx
+    written."""
+    e = ESZ[w.dtype]
+    n = w.batches * w.heads * w.sq * w.sk
+    if pass_ == "bwd":
+        return 3 * n * e
+    kept = n
+    if w.mask == "causal":
+        kept = w.batches * w.heads * w.sq * (w.sq + 1) // 2
+    elif w.mask == "causal_aligned":
+        per = sum(min(max(i + 1 + w.sk - w.sq, 0), w.sk) for i in range(w.sq))
+        kept = w.batches * w.heads * per
+    b = kept * e + n * e
+    if w.mask == "padding":
+        b += w.mask_batches * w.sq * w.sk
+    return b
+
+
+def run_softmax_detail(ops, args, flush, dev, peak):
+    from rmsnorm_fp8_quantization_gb300.workloads import SOFTMAX_WORKLOADS, make_softmax_inputs
+    out = {}
+    steps = max(5, args.steps // 2)
+    for name, w in SOFTMAX_WORKLOADS.items():
+        inp = make_softmax_inputs(w, seed=0, device=str(dev))
+        y = torch.empty_like(inp["x"])
+        dx = torch.empty_like(inp["x"])
+
+        def fwd():
+            ops.softmax_fwd(inp["x"], w.scale, w.mask, inp["mask"], out=y)
+
+        def bwd():
+            ops.softmax_bwd(inp["dy"], y, w.scale, out=dx)
+
+        per, _ = time_calls([fwd, bwd], steps, 3)
+        fper, _ = time_calls([fwd, bwd], steps, 3, flush)
+        d = {}
+        for lab, ts, fts in zip(("fwd", "bwd"), per, fper):
+            ms = statistics.median(ts)
+            nb = softmax_bytes(w, lab)
+            gbs = nb / (ms / 1e3) / 1e9
+            d[lab] = {"us": ms * 1e3, "us_l2_flushed": statistics.median(fts) * 1e3,
+                      "bytes": nb, "gbs": gbs, "frac_of_peak": gbs / peak,
+                      "frac_of_8tbs": gbs / NOMINAL_HBM_GBS}
+        out[name] = d
+        del inp, y, dx
         torch.cuda.empty_cache()
     return out
 

@@ -137,17 +137,30 @@ __global__ void __launch_bounds__(kSmThreads) softmax_fwd_kernel(const SmFwdPara
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
     const int j0 = (k * gthreads + t) * V;
-    if (live && j0 < sk) {
+    // Causal rows: loads wholly past the last kept key are skipped.
+    if (live && j0 < limit) {
       load_v<T, V>(xr + j0, u[k]);
     } else {
 #pragma unroll
       for (int e = 0; e < V; ++e) u[k][e] = 0.f;
     }
+    uint64_t mbits = 0;  // padding: the V mask bytes of this load
+    if constexpr (MASK == 1) {
+      if (live && j0 < sk) {
+        if constexpr (V == 8) {
+          mbits = *reinterpret_cast<const uint64_t*>(mr + j0);
+        } else if constexpr (V == 4) {
+          mbits = *reinterpret_cast<const uint32_t*>(mr + j0);
+        } else {
+          mbits = mr[j0];
+        }
+      }
+    }
 #pragma unroll
     for (int e = 0; e < V; ++e) {
       const int j = j0 + e;
       bool keep = live && j < limit;
-      if constexpr (MASK == 1) keep = keep && mr[j] == 0;
+      if constexpr (MASK == 1) keep = keep && ((mbits >> (8 * e)) & 0xFFu) == 0;
       u[k][e] = keep ? u[k][e] * p.scale_log2e : -INFINITY;
       m = fmaxf(m, u[k][e]);
     }
@@ -187,9 +200,41 @@ struct SmBwdParams {
   float scale;
 };
 
+// Loads V consecutive elements as raw 32-bit words (V >= 2: 16 bytes).
+template <typename T, int V>
+__device__ __forceinline__ void load_words(const T* p, uint32_t* w) {
+  if constexpr (V == 1) {
+    w[0] = __float_as_uint(SmElem<T>::get(p));
+  } else {
+    const uint4 u = ld_stream16(p);
+    w[0] = u.x;
+    w[1] = u.y;
+    w[2] = u.z;
+    w[3] = u.w;
+  }
+}
+template <typename T, int V>
+__device__ __forceinline__ void words_to_floats(const uint32_t* w, float* f) {
+  if constexpr (V == 1) {
+    f[0] = __uint_as_float(w[0]);
+  } else {
+    uint64_t pr[V / 2];
+    widen_pairs<T, V>(w, pr);
+#pragma unroll
+    for (int i = 0; i < V / 2; ++i) {
+      const float2 t = u2(pr[i]);
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  }
+}
+
+// Backward: y and dy stay packed in registers between the dot product and
+// the output pass (widened twice), which keeps the register count low.
 template <typename T, int V, int NV>
-__global__ void __launch_bounds__(kSmThreads) softmax_bwd_kernel(const SmBwdParams p) {
+__global__ void __launch_bounds__(kSmThreads, 3) softmax_bwd_kernel(const SmBwdParams p) {
   pdl_begin();
+  constexpr int NW = V == 1 ? 1 : 4;
   __shared__ float buf[kSmThreads / 32];
   const int gthreads = 32 * p.wpr;
   const int rows_per_cta = kSmThreads / gthreads;
@@ -200,20 +245,26 @@ __global__ void __launch_bounds__(kSmThreads) softmax_bwd_kernel(const SmBwdPara
   const int64_t rr = live ? row : 0;
   const T* yr = reinterpret_cast<const T*>(p.y) + rr * sk;
   const T* dr = reinterpret_cast<const T*>(p.dy) + rr * sk;
-  float yv[NV][V], dv[NV][V];
-  float c = 0.f;
+  uint32_t yw[NV][NW], dw[NV][NW];
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
     const int j0 = (k * gthreads + t) * V;
     if (live && j0 < sk) {
-      load_v<T, V>(yr + j0, yv[k]);
-      load_v<T, V>(dr + j0, dv[k]);
+      load_words<T, V>(yr + j0, yw[k]);
+      load_words<T, V>(dr + j0, dw[k]);
     } else {
 #pragma unroll
-      for (int e = 0; e < V; ++e) yv[k][e] = dv[k][e] = 0.f;
+      for (int e = 0; e < NW; ++e) yw[k][e] = dw[k][e] = 0u;
     }
+  }
+  float c = 0.f;
 #pragma unroll
-    for (int e = 0; e < V; ++e) c = fmaf(yv[k][e], dv[k][e], c);
+  for (int k = 0; k < NV; ++k) {
+    float yv[V], dv[V];
+    words_to_floats<T, V>(yw[k], yv);
+    words_to_floats<T, V>(dw[k], dv);
+#pragma unroll
+    for (int e = 0; e < V; ++e) c = fmaf(yv[e], dv[e], c);
   }
   c = group_reduce<false>(c, buf, p.wpr);
   T* xr = reinterpret_cast<T*>(p.dx) + rr * sk;
@@ -221,9 +272,11 @@ __global__ void __launch_bounds__(kSmThreads) softmax_bwd_kernel(const SmBwdPara
   for (int k = 0; k < NV; ++k) {
     const int j0 = (k * gthreads + t) * V;
     if (live && j0 < sk) {
-      float o[V];
+      float yv[V], dv[V], o[V];
+      words_to_floats<T, V>(yw[k], yv);
+      words_to_floats<T, V>(dw[k], dv);
 #pragma unroll
-      for (int e = 0; e < V; ++e) o[e] = p.scale * yv[k][e] * (dv[k][e] - c);
+      for (int e = 0; e < V; ++e) o[e] = p.scale * yv[e] * (dv[e] - c);
       store_v<T, V>(xr + j0, o);
     }
   }
@@ -300,7 +353,8 @@ gbn_status gbn_softmax_fwd(const void* x, const uint8_t* mask, void* y, int64_t 
   if (!x || !y) return GBN_ERR_NULL;
   if (mask_kind == GBN_SOFTMAX_PADDING && (!mask || mask_batches < 1)) return GBN_ERR_NULL;
   const int vec = 16 / sm_esize(dtype);
-  const bool vok = sk % vec == 0 && sm_aligned(x) && sm_aligned(y);
+  const bool vok = sk % vec == 0 && sm_aligned(x) && sm_aligned(y) &&
+                   (mask_kind != GBN_SOFTMAX_PADDING || sm_aligned(mask));
   int nv = 0, wpr = 0;
   if (!sm_geom(static_cast<int>(sk), vok ? vec : 1, &nv, &wpr)) return GBN_ERR_SHAPE;
   SmFwdParams p{x, mask, y, rows, heads * sq, sq, mask_batches, static_cast<int>(sk), wpr,
@@ -330,6 +384,12 @@ gbn_status gbn_softmax_bwd(const void* dy, const void* y, void* dx, int64_t rows
   const bool vok = sk % vec == 0 && sm_aligned(dy) && sm_aligned(y) && sm_aligned(dx);
   int nv = 0, wpr = 0;
   if (!sm_geom(static_cast<int>(sk), vok ? vec : 1, &nv, &wpr)) return GBN_ERR_SHAPE;
+  // Two packed rows per load stay in registers: at most 4 loads per thread
+  // (more warps per row instead), so the kernel keeps three CTAs per SM.
+  if (nv == 8 && wpr < kSmThreads / 32) {
+    nv = 4;
+    wpr *= 2;
+  }
   SmBwdParams p{dy, y, dx, rows, static_cast<int>(sk), wpr, scale};
   const int64_t rows_per_cta = kSmThreads / (32 * wpr);
   const int64_t grid = (rows + rows_per_cta - 1) / rows_per_cta;
