@@ -16,6 +16,9 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <map>
+#include <mutex>
+
 #include "gbnorm.h"
 #include "gbn_device.cuh"
 
@@ -108,98 +111,6 @@ struct SmFwdParams {
   float scale_log2e;
 };
 
-// Forward.  MASK: 0 none, 1 padding mask, 2 upper-triangular, 3 aligned causal.
-template <typename T, int V, int NV, int MASK>
-__global__ void __launch_bounds__(kSmThreads) softmax_fwd_kernel(const SmFwdParams p) {
-  pdl_begin();
-  __shared__ float buf[kSmThreads / 32];
-  const int gthreads = 32 * p.wpr;
-  const int rows_per_cta = kSmThreads / gthreads;
-  const int g = threadIdx.x / gthreads, t = threadIdx.x % gthreads;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * rows_per_cta + g;
-  const bool live = row < p.rows;
-  const int sk = p.sk;
-  const int64_t rr = live ? row : 0;
-  const int64_t i = rr % p.sq;  // query index
-  int limit = sk;               // causal: positions j < limit are kept
-  if constexpr (MASK == 2) limit = static_cast<int>(i) + 1;
-  if constexpr (MASK == 3) {
-    const int64_t l = i + 1 + (sk - p.sq);
-    limit = l < 0 ? 0 : (l > sk ? sk : static_cast<int>(l));
-  }
-  const T* xr = reinterpret_cast<const T*>(p.x) + rr * sk;
-  const uint8_t* mr = nullptr;
-  if constexpr (MASK == 1)
-    mr = p.mask + ((rr / p.heads_sq) % p.mask_batches * p.sq + i) * static_cast<int64_t>(sk);
-
-  float u[NV][V];
-  float m = -INFINITY;
-#pragma unroll
-  for (int k = 0; k < NV; ++k) {
-    const int j0 = (k * gthreads + t) * V;
-    // Causal rows: loads wholly past the last kept key are skipped.
-    if (live && j0 < limit) {
-      load_v<T, V>(xr + j0, u[k]);
-    } else {
-#pragma unroll
-      for (int e = 0; e < V; ++e) u[k][e] = 0.f;
-    }
-    uint64_t mbits = 0;  // padding: the V mask bytes of this load
-    if constexpr (MASK == 1) {
-      if (live && j0 < sk) {
-        if constexpr (V == 8) {
-          mbits = *reinterpret_cast<const uint64_t*>(mr + j0);
-        } else if constexpr (V == 4) {
-          mbits = *reinterpret_cast<const uint32_t*>(mr + j0);
-        } else {
-          mbits = mr[j0];
-        }
-      }
-    }
-#pragma unroll
-    for (int e = 0; e < V; ++e) {
-      const int j = j0 + e;
-      bool keep = live && j < limit;
-      if constexpr (MASK == 1) keep = keep && ((mbits >> (8 * e)) & 0xFFu) == 0;
-      u[k][e] = keep ? u[k][e] * p.scale_log2e : -INFINITY;
-      m = fmaxf(m, u[k][e]);
-    }
-  }
-  m = group_reduce<true>(m, buf, p.wpr);
-  const float mo = m == -INFINITY ? 0.f : m;  // nothing kept: every term is exp2(-inf) = 0
-  float s = 0.f;
-#pragma unroll
-  for (int k = 0; k < NV; ++k) {
-#pragma unroll
-    for (int e = 0; e < V; ++e) {
-      u[k][e] = exp2f(u[k][e] - mo);
-      s += u[k][e];
-    }
-  }
-  s = group_reduce<false>(s, buf, p.wpr);
-  const float inv = s > 0.f ? 1.f / s : 0.f;
-  T* yr = reinterpret_cast<T*>(p.y) + rr * sk;
-#pragma unroll
-  for (int k = 0; k < NV; ++k) {
-    const int j0 = (k * gthreads + t) * V;
-    if (live && j0 < sk) {
-#pragma unroll
-      for (int e = 0; e < V; ++e) u[k][e] *= inv;
-      store_v<T, V>(yr + j0, u[k]);
-    }
-  }
-}
-
-struct SmBwdParams {
-  const void* dy;
-  const void* y;
-  void* dx;
-  int64_t rows;
-  int sk;
-  int wpr;
-  float scale;
-};
-
 // Loads V consecutive elements as raw 32-bit words (V >= 2: 16 bytes).
 template <typename T, int V>
 __device__ __forceinline__ void load_words(const T* p, uint32_t* w) {
@@ -228,6 +139,145 @@ __device__ __forceinline__ void words_to_floats(const uint32_t* w, float* f) {
     }
   }
 }
+
+// Forward.  MASK: 0 none, 1 padding mask, 2 upper-triangular, 3 aligned
+// causal.  The CTA walks blocks of rows_per_cta rows (blockIdx, blockIdx +
+// gridDim, ...).  With the most loads per thread (NV = 8) the grid is
+// persistent and the next block's packed row (and mask bytes) is loaded into
+// registers while the current one is computed; with fewer, one block per CTA
+// and more CTAs resident (fewer registers) keep enough bytes in flight.
+template <typename T, int V, int NV, int MASK>
+__global__ void __launch_bounds__(kSmThreads, NV == 8 ? 2 : 4)
+    softmax_fwd_kernel(const SmFwdParams p) {
+  pdl_begin();
+  constexpr int NW = V == 1 ? 1 : 4;
+  __shared__ float buf[kSmThreads / 32];
+  const int gthreads = 32 * p.wpr;
+  const int rows_per_cta = kSmThreads / gthreads;
+  const int g = threadIdx.x / gthreads, t = threadIdx.x % gthreads;
+  const int sk = p.sk;
+  const int64_t nblocks = (p.rows + rows_per_cta - 1) / rows_per_cta;
+
+  // Positions j < limit of row `row` may be kept (causal rows end early).
+  auto row_limit = [&](int64_t row) {
+    int limit = sk;
+    const int64_t i = row % p.sq;
+    if constexpr (MASK == 2) limit = static_cast<int>(i) + 1;
+    if constexpr (MASK == 3) {
+      const int64_t l = i + 1 + (sk - p.sq);
+      limit = l < 0 ? 0 : (l > sk ? sk : static_cast<int>(l));
+    }
+    return limit;
+  };
+  auto fetch = [&](int64_t blk, uint32_t (&w)[NV][NW], uint64_t (&mb)[NV]) {
+    const int64_t row = blk * rows_per_cta + g;
+    const bool live = blk < nblocks && row < p.rows;
+    const int limit = live ? row_limit(row) : 0;
+    const T* xr = reinterpret_cast<const T*>(p.x) + (live ? row : 0) * sk;
+    const uint8_t* mr = nullptr;
+    if constexpr (MASK == 1)
+      mr = p.mask + ((live ? row : 0) / p.heads_sq % p.mask_batches * p.sq +
+                     (live ? row : 0) % p.sq) * static_cast<int64_t>(sk);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int j0 = (k * gthreads + t) * V;
+      mb[k] = 0;
+      if (j0 < limit) {
+        load_words<T, V>(xr + j0, w[k]);
+        if constexpr (MASK == 1) {
+          if constexpr (V == 8) {
+            mb[k] = *reinterpret_cast<const uint64_t*>(mr + j0);
+          } else if constexpr (V == 4) {
+            mb[k] = *reinterpret_cast<const uint32_t*>(mr + j0);
+          } else {
+            mb[k] = mr[j0];
+          }
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < NW; ++e) w[k][e] = 0u;
+      }
+    }
+  };
+
+  // Softmax of the block's row from its packed loads w and mask bytes mb.
+  auto compute = [&](int64_t blk, const uint32_t (&w)[NV][NW], const uint64_t (&mb)[NV]) {
+    const int64_t row = blk * rows_per_cta + g;
+    const bool live = row < p.rows;
+    const int limit = live ? row_limit(row) : 0;
+    float u[NV][V];
+    float m = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int j0 = (k * gthreads + t) * V;
+      words_to_floats<T, V>(w[k], u[k]);
+#pragma unroll
+      for (int e = 0; e < V; ++e) {
+        bool keep = j0 + e < limit;
+        if constexpr (MASK == 1) keep = keep && ((mb[k] >> (8 * e)) & 0xFFu) == 0;
+        u[k][e] = keep ? u[k][e] * p.scale_log2e : -INFINITY;
+        m = fmaxf(m, u[k][e]);
+      }
+    }
+    m = group_reduce<true>(m, buf, p.wpr);
+    const float mo = m == -INFINITY ? 0.f : m;  // nothing kept: every term is exp2(-inf) = 0
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+#pragma unroll
+      for (int e = 0; e < V; ++e) {
+        u[k][e] = exp2f(u[k][e] - mo);
+        s += u[k][e];
+      }
+    }
+    s = group_reduce<false>(s, buf, p.wpr);
+    const float inv = s > 0.f ? 1.f / s : 0.f;
+    T* yr = reinterpret_cast<T*>(p.y) + (live ? row : 0) * sk;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int j0 = (k * gthreads + t) * V;
+      if (live && j0 < sk) {
+#pragma unroll
+        for (int e = 0; e < V; ++e) u[k][e] *= inv;
+        store_v<T, V>(yr + j0, u[k]);
+      }
+    }
+  };
+
+  uint32_t cw[NV][NW];
+  uint64_t cm[NV];
+  if constexpr (NV < 8) {
+    // One block per CTA.
+    fetch(blockIdx.x, cw, cm);
+    compute(blockIdx.x, cw, cm);
+  } else {
+    // Persistent, the next block's loads in flight during this one.
+    int64_t blk = blockIdx.x;
+    fetch(blk, cw, cm);
+    for (; blk < nblocks; blk += gridDim.x) {
+      uint32_t nw[NV][NW];
+      uint64_t nm[NV];
+      fetch(blk + gridDim.x, nw, nm);
+      compute(blk, cw, cm);
+#pragma unroll
+      for (int k = 0; k < NV; ++k) {
+#pragma unroll
+        for (int e = 0; e < NW; ++e) cw[k][e] = nw[k][e];
+        cm[k] = nm[k];
+      }
+    }
+  }
+}
+
+struct SmBwdParams {
+  const void* dy;
+  const void* y;
+  void* dx;
+  int64_t rows;
+  int sk;
+  int wpr;
+  float scale;
+};
 
 // Backward: y and dy stay packed in registers between the dot product and
 // the output pass (widened twice), which keeps the register count low.
@@ -299,24 +349,43 @@ bool sm_geom(int sk, int v, int* nv, int* wpr) {
   return false;
 }
 
+using SmFwdKernel = void (*)(const SmFwdParams);
+
 template <typename T, int V, int NV>
-cudaError_t launch_fwd_nv(const SmFwdParams& p, int mask, int grid, cudaStream_t st) {
+SmFwdKernel fwd_kernel_nv(int mask) {
   switch (mask) {
-    case 0: return launch_pdl(softmax_fwd_kernel<T, V, NV, 0>, dim3(grid), dim3(kSmThreads), 0, st, p);
-    case 1: return launch_pdl(softmax_fwd_kernel<T, V, NV, 1>, dim3(grid), dim3(kSmThreads), 0, st, p);
-    case 2: return launch_pdl(softmax_fwd_kernel<T, V, NV, 2>, dim3(grid), dim3(kSmThreads), 0, st, p);
-    default: return launch_pdl(softmax_fwd_kernel<T, V, NV, 3>, dim3(grid), dim3(kSmThreads), 0, st, p);
+    case 0: return softmax_fwd_kernel<T, V, NV, 0>;
+    case 1: return softmax_fwd_kernel<T, V, NV, 1>;
+    case 2: return softmax_fwd_kernel<T, V, NV, 2>;
+    default: return softmax_fwd_kernel<T, V, NV, 3>;
   }
 }
 
 template <typename T, int V>
-cudaError_t launch_fwd(const SmFwdParams& p, int mask, int nv, int grid, cudaStream_t st) {
+SmFwdKernel fwd_kernel(int mask, int nv) {
   switch (nv) {
-    case 1: return launch_fwd_nv<T, V, 1>(p, mask, grid, st);
-    case 2: return launch_fwd_nv<T, V, 2>(p, mask, grid, st);
-    case 4: return launch_fwd_nv<T, V, 4>(p, mask, grid, st);
-    default: return launch_fwd_nv<T, V, 8>(p, mask, grid, st);
+    case 1: return fwd_kernel_nv<T, V, 1>(mask);
+    case 2: return fwd_kernel_nv<T, V, 2>(mask);
+    case 4: return fwd_kernel_nv<T, V, 4>(mask);
+    default: return fwd_kernel_nv<T, V, 8>(mask);
   }
+}
+
+// Resident CTAs per SM of a forward kernel (cached per device and kernel).
+int fwd_ctas_per_sm(SmFwdKernel k) {
+  static std::mutex mu;
+  static std::map<std::pair<int, SmFwdKernel>, int> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = cache.find({dev, k});
+  if (it != cache.end()) return it->second;
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kSmThreads, 0) != cudaSuccess)
+    occ = 0;
+  if (occ < 1) occ = 1;
+  cache[{dev, k}] = occ;
+  return occ;
 }
 
 template <typename T, int V>
@@ -331,6 +400,8 @@ cudaError_t launch_bwd(const SmBwdParams& p, int nv, int grid, cudaStream_t st) 
 }
 
 int sm_esize(gbn_dtype d) { return d == GBN_F32 ? 4 : 2; }
+
+
 bool sm_aligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
@@ -359,18 +430,28 @@ gbn_status gbn_softmax_fwd(const void* x, const uint8_t* mask, void* y, int64_t 
   if (!sm_geom(static_cast<int>(sk), vok ? vec : 1, &nv, &wpr)) return GBN_ERR_SHAPE;
   SmFwdParams p{x, mask, y, rows, heads * sq, sq, mask_batches, static_cast<int>(sk), wpr,
                 scale * kLog2e};
-  const int64_t rows_per_cta = kSmThreads / (32 * wpr);
-  const int64_t grid = (rows + rows_per_cta - 1) / rows_per_cta;
-  if (grid > 0x7FFFFFFF) return GBN_ERR_SHAPE;
-  const int m = static_cast<int>(mask_kind), g = static_cast<int>(grid);
-  cudaError_t e;
+  const int m = static_cast<int>(mask_kind);
+  SmFwdKernel k;
   if (dtype == GBN_F32)
-    e = vok ? launch_fwd<float, 4>(p, m, nv, g, stream) : launch_fwd<float, 1>(p, m, nv, g, stream);
+    k = vok ? fwd_kernel<float, 4>(m, nv) : fwd_kernel<float, 1>(m, nv);
   else if (dtype == GBN_BF16)
-    e = vok ? launch_fwd<__nv_bfloat16, 8>(p, m, nv, g, stream)
-            : launch_fwd<__nv_bfloat16, 1>(p, m, nv, g, stream);
+    k = vok ? fwd_kernel<__nv_bfloat16, 8>(m, nv) : fwd_kernel<__nv_bfloat16, 1>(m, nv);
   else
-    e = vok ? launch_fwd<__half, 8>(p, m, nv, g, stream) : launch_fwd<__half, 1>(p, m, nv, g, stream);
+    k = vok ? fwd_kernel<__half, 8>(m, nv) : fwd_kernel<__half, 1>(m, nv);
+  const int64_t rows_per_cta = kSmThreads / (32 * wpr);
+  int64_t grid = (rows + rows_per_cta - 1) / rows_per_cta;
+  // NV = 8: persistent, at most the CTAs that are resident at once.
+  if (nv == 8) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return GBN_ERR_CUDA;
+    const int64_t resident = static_cast<int64_t>(sms) * fwd_ctas_per_sm(k);
+    if (grid > resident) grid = resident;
+  }
+  if (grid > 0x7FFFFFFF) return GBN_ERR_SHAPE;
+  const cudaError_t e =
+      launch_pdl(k, dim3(static_cast<unsigned>(grid)), dim3(kSmThreads), 0, stream, p);
   return e == cudaSuccess ? GBN_OK : GBN_ERR_CUDA;
 }
 
