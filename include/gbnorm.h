@@ -227,6 +227,14 @@ gbn_status gbn_norm_bwd_noalloc(const void* dz, const void* x, const float* mu,
 #define GBN_DEVICE_ERR_COPY_TIMEOUT 1u
 gbn_status gbn_device_error(unsigned int* flags, int clear);
 
+/* Self-test of that failure path (no counterpart on the pages): enqueues on
+ * `stream` a one-thread kernel that waits for 16 bytes on an mbarrier that no
+ * copy will ever fill, gives up after timeout_us microseconds (1 .. 2e6, else
+ * GBN_ERR_SHAPE) and sets GBN_DEVICE_ERR_COPY_TIMEOUT, exactly as a kernel
+ * whose bulk copy never landed would.  Nothing faults or traps; the context
+ * stays usable. */
+gbn_status gbn_selftest_copy_timeout(unsigned int timeout_us, cudaStream_t stream);
+
 /* ---- Scaled (masked) softmax ("Migrate norms and softmax kernels to NVRTC",
  * Description and JIT cost table: scaled_masked_softmax,
  * scaled_upper_triang_masked_softmax, scaled_aligned_causal_masked_softmax,

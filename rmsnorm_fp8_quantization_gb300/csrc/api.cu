@@ -638,6 +638,13 @@ gbn_status gbn_norm_bwd(const void* dz, const void* x, const float* mu, const fl
   return launch_bwd_finalize(f, stream) == cudaSuccess ? GBN_OK : GBN_ERR_CUDA;
 }
 
+gbn_status gbn_selftest_copy_timeout(unsigned int timeout_us, cudaStream_t stream) {
+  if (timeout_us < 1 || timeout_us > 2000000u) return GBN_ERR_SHAPE;
+  const cudaError_t e =
+      kernels_f32().probe_copy_timeout(static_cast<unsigned long long>(timeout_us) * 1000ull, stream);
+  return e == cudaSuccess ? GBN_OK : GBN_ERR_CUDA;
+}
+
 gbn_status gbn_device_error(unsigned int* flags, int clear) {
   if (!flags) return GBN_ERR_NULL;
   unsigned int a = 0, b = 0, c = 0;

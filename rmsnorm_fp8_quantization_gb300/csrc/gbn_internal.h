@@ -165,6 +165,9 @@ struct KernelTable {
   cudaError_t (*bwd_cluster_launch)(bool layernorm, bool add, int cluster, int threads,
                                     int stages, int smem, int hc, const BwdParams& p,
                                     int clusters, cudaStream_t stream);
+  // Self-test: a kernel whose wait for a copy that is never issued gives up
+  // after limit_ns and sets this translation unit's device error flag.
+  cudaError_t (*probe_copy_timeout)(unsigned long long limit_ns, cudaStream_t stream);
   // Sticky device-side error bits of this translation unit's kernels.
   cudaError_t (*read_device_error)(unsigned int* value, bool clear);
 };

@@ -10,7 +10,7 @@ const KernelTable& kernels_bf16() {
       &L::bwd_generic_occupancy, &L::bwd_generic_launch, &L::fwd_ring_occupancy,
       &L::fwd_ring_launch,       &L::bwd_ring_occupancy, &L::bwd_ring_launch,
       &L::fwd_cluster_max_clusters, &L::fwd_cluster_launch, &L::bwd_cluster_max_clusters,
-      &L::bwd_cluster_launch,       &L::read_device_error};
+      &L::bwd_cluster_launch,       &L::probe_copy_timeout,     &L::read_device_error};
   return table;
 }
 

@@ -252,6 +252,10 @@ struct Launch {
     return cudaGetLastError();
   }
 
+  static cudaError_t probe_copy_timeout(unsigned long long limit_ns, cudaStream_t st) {
+    return launch_pdl(copy_timeout_probe_kernel, dim3(1), dim3(32), 0, st, limit_ns);
+  }
+
   static cudaError_t read_device_error(unsigned int* v, bool clear) {
     cudaError_t e = cudaMemcpyFromSymbol(v, g_gbn_device_error, sizeof(unsigned int));
     if (e != cudaSuccess || !clear) return e;

@@ -25,6 +25,20 @@ constexpr int kMaxRingStages = 8;
 // own bulk copies exceeded kWaitLimitNs and the kernel stopped early.
 static __device__ unsigned int g_gbn_device_error;
 
+// Self-test of the bounded wait: one thread waits for 16 bytes on an
+// mbarrier that no copy will ever fill, gives up after limit_ns and records
+// the timeout in the device error flag, as a real kernel would.
+static __global__ void copy_timeout_probe_kernel(const unsigned long long limit_ns) {
+  pdl_begin();
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&bar, 16u);
+    if (!mbar_wait_for(&bar, 0u, limit_ns)) atomicOr(&g_gbn_device_error, 1u);
+  }
+}
+
 // Per-CTA schedule: this CTA owns rows first, first + stride, ...
 struct RowSchedule {
   int64_t first, stride, count;

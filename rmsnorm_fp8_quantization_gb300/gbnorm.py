@@ -29,7 +29,7 @@ TORCH_DTYPE = {torch.float32: GBN_F32, torch.bfloat16: GBN_BF16, torch.float16: 
 
 FUNCTIONS = ("gbn_norm_fwd_workspace_size", "gbn_norm_fwd", "gbn_norm_bwd_workspace_size",
              "gbn_norm_bwd", "gbn_norm_bwd_noalloc", "gbn_device_error", "gbn_status_string",
-             "gbn_softmax_fwd", "gbn_softmax_bwd")
+             "gbn_softmax_fwd", "gbn_softmax_bwd", "gbn_selftest_copy_timeout")
 (GBN_SOFTMAX_NO_MASK, GBN_SOFTMAX_PADDING, GBN_SOFTMAX_CAUSAL_UPPER,
  GBN_SOFTMAX_CAUSAL_ALIGNED) = range(4)
 GBN_SOFTMAX_MAX_KEYS = 16384
@@ -68,6 +68,8 @@ def _load():
     lib.gbn_softmax_fwd.restype = I
     lib.gbn_softmax_bwd.argtypes = [P, P, P, I64, I64, I, F, P]
     lib.gbn_softmax_bwd.restype = I
+    lib.gbn_selftest_copy_timeout.argtypes = [ctypes.c_uint, P]
+    lib.gbn_selftest_copy_timeout.restype = I
     lib.gbn_status_string.argtypes = [I]
     lib.gbn_status_string.restype = ctypes.c_char_p
     return lib
@@ -172,3 +174,8 @@ def gbn_softmax_fwd(x, mask, y, batches, heads, sq, sk, mask_batches, dtype, mas
 def gbn_softmax_bwd(dy, y, dx, rows, sk, dtype, scale, stream=None) -> int:
     return _lib.gbn_softmax_bwd(_ptr(dy), _ptr(y), _ptr(dx), rows, sk, dtype, float(scale),
                                 _stream(stream))
+
+
+def gbn_selftest_copy_timeout(timeout_us, stream=None) -> int:
+    """Enqueues the bounded-wait self-test kernel (see include/gbnorm.h)."""
+    return _lib.gbn_selftest_copy_timeout(int(timeout_us), _stream(stream))
