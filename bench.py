@@ -587,12 +587,27 @@ def run_reference(args):
 
 
 def run_only(args):
-    """A short run of one workload's passes (the command profiled by ncu)."""
+    """A short run of one workload's passes (the command profiled by ncu).
+    Softmax workloads: --rows overrides the batch count."""
     from rmsnorm_fp8_quantization_gb300 import _build
     _build.build()
     from rmsnorm_fp8_quantization_gb300 import ops
-    from rmsnorm_fp8_quantization_gb300.workloads import WORKLOADS, make_inputs
+    from rmsnorm_fp8_quantization_gb300.workloads import (SOFTMAX_WORKLOADS, WORKLOADS,
+                                                          make_inputs, make_softmax_inputs)
     torch.cuda.set_device(0)
+    if args.only in SOFTMAX_WORKLOADS:
+        w = SOFTMAX_WORKLOADS[args.only]
+        if args.rows:
+            w = w.with_shape(args.rows, w.heads, w.sq, w.sk)
+        inp = make_softmax_inputs(w, seed=0, device="cuda")
+        y = torch.empty_like(inp["x"])
+        dx = torch.empty_like(inp["x"])
+        calls = [lambda: ops.softmax_fwd(inp["x"], w.scale, w.mask, inp["mask"], out=y),
+                 lambda: ops.softmax_bwd(inp["dy"], y, w.scale, out=dx)]
+        per, _ = time_calls(calls, args.steps, args.warmup)
+        print(json.dumps({"workload": w.name, "batches": w.batches,
+                          "us": [statistics.median(t) * 1e3 for t in per]}))
+        return
     w = WORKLOADS[args.only]
     if args.rows:
         w = w.with_shape(args.rows)

@@ -59,6 +59,10 @@ WORKLOADS = {
     "ln_bf16_16384x4000": Workload(
         "ln_bf16_16384x4000", "layernorm", 16384, 4000, "bf16", "f32", 1e-5,
         x_mean=0.5, x_std=2.0, beta_std=0.1),
+    # Long rows (each split over a thread-block cluster): LayerNorm fwd+bwd, 4096 x 65536.
+    "ln_bf16_4096x65536": Workload(
+        "ln_bf16_4096x65536", "layernorm", 4096, 65536, "bf16", "f32", 1e-5,
+        x_mean=0.5, x_std=2.0, beta_std=0.1),
     # RMSNorm fwd bf16 -> E4M3, delayed per-tensor scaling, rowwise + transposed colwise.
     "rms_bf16_e4m3_delayed_32768x8192": Workload(
         "rms_bf16_e4m3_delayed_32768x8192", "rmsnorm", 32768, 8192, "bf16", "bf16", 1e-6,
