@@ -109,3 +109,37 @@ def test_shape_errors(gpu):
     with pytest.raises(GbnError):   # upper-triangular needs sq == sk
         gpu.softmax_fwd(torch.zeros(1, 1, 4, 8, dtype=torch.bfloat16, device="cuda"),
                         mask_kind="causal")
+
+
+def test_softmax_graph_capture_and_guard_bands(gpu):
+    w = wl(2, 2, 128, 2048, mask="causal_aligned")
+    inp = make_softmax_inputs(w)
+    x, dy = inp["x"].cuda(), inp["dy"].cuda()
+    n = x.numel()
+    G = 2048
+    ybuf = torch.full((n + 2 * G,), 7.0, dtype=x.dtype, device="cuda")
+    y = ybuf[G:G + n].view(x.shape)
+    dxbuf = torch.full((n + 2 * G,), 7.0, dtype=x.dtype, device="cuda")
+    dx = dxbuf[G:G + n].view(x.shape)
+
+    def step():
+        gpu.softmax_fwd(x, w.scale, w.mask, out=y)
+        gpu.softmax_bwd(dy, y, w.scale, out=dx)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    eager = (y.clone(), dx.clone())
+    y.zero_()
+    dx.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(eager[0], y) and torch.equal(eager[1], dx)
+    for buf in (ybuf, dxbuf):
+        assert torch.all(buf[:G] == 7.0) and torch.all(buf[G + n:] == 7.0), "guard band written"
