@@ -1,7 +1,8 @@
 /*
- * gbnorm — fused LayerNorm / RMSNorm forward and backward for GB300 (sm_103a).
+ * gbnorm — fused LayerNorm / RMSNorm forward and backward (and the scaled
+ * masked softmax) for GB300 (sm_103a).
  *
- * C ABI of libgbnorm.so.  The operations follow two pages:
+ * C ABI of libgbnorm.so.  The norm operations follow two pages:
  *   "Implementation:NVIDIA TransformerEngine JAX XLA Normalization"
  *     (sections Description, Signature, I/O Contract): the forward handler's
  *     buffers (input, gamma, beta, scale, amax; output, colwise output, mu,
@@ -12,6 +13,8 @@
  *   "Implementation:NVIDIA TransformerEngine Ops Fused Backward Add RMSNorm"
  *     (sections Description, I/O Contract): the backward with the residual
  *     gradient added to the input gradient in the same kernel.
+ * The softmax entry points (end of this file) follow "Migrate norms and
+ * softmax kernels to NVRTC" (Description, JIT cost table), which names them.
  *
  * Arithmetic (x is one row of `hidden` elements; all device math in fp32):
  *   LayerNorm: mu = mean(x); var = mean((x - mu)^2); rsigma = 1/sqrt(var + eps)
@@ -39,10 +42,12 @@
  *     multiple of the 16-byte vector) are accepted and take a scalar path.
  *   - SM margin: the persistent grids use (SM count - sm_margin) SMs, at
  *     least one, times the kernel's occupancy.
- *   - 1 <= hidden <= 2^24 and rows >= 0 (else GBN_ERR_SHAPE).  Rows that do
- *     not fit the register-resident kernels (e.g. hidden > 65536 for bf16)
- *     run on a slower generic kernel.
- *   - Outputs must not alias inputs.
+ *   - 1 <= hidden <= 2^24 and rows >= 0 (else GBN_ERR_SHAPE).  Rows of up to
+ *     16384 two-byte (8192 four-byte) elements run on one CTA each; longer
+ *     rows are split over a thread-block cluster of up to 8 CTAs (forward up
+ *     to 131072 / 65536 elements, backward up to 65536 / 32768); longer
+ *     still, or misaligned, they run on a slower generic kernel.
+ *   - Norm outputs must not alias inputs.
  */
 #ifndef GBNORM_H_
 #define GBNORM_H_

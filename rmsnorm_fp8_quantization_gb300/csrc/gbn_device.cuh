@@ -287,26 +287,6 @@ __device__ __forceinline__ uint8_t e4m3(float v) {
   return static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
 }
 
-// Packs N (multiple of 4) E4M3 codes of v[i] * s into N/4 words.
-template <int N>
-__device__ __forceinline__ void e4m3_pack_scaled(const float* v, float s, uint32_t* w) {
-#pragma unroll
-  for (int i = 0; i < N / 4; ++i) {
-    const uint32_t a = e4m3x2(v[4 * i] * s, v[4 * i + 1] * s);
-    const uint32_t b = e4m3x2(v[4 * i + 2] * s, v[4 * i + 3] * s);
-    w[i] = a | (b << 16);
-  }
-}
-// Same with a per-element multiplier.
-template <int N>
-__device__ __forceinline__ void e4m3_pack_mul(const float* v, const float* s, uint32_t* w) {
-#pragma unroll
-  for (int i = 0; i < N / 4; ++i) {
-    const uint32_t a = e4m3x2(v[4 * i] * s[4 * i], v[4 * i + 1] * s[4 * i + 1]);
-    const uint32_t b = e4m3x2(v[4 * i + 2] * s[4 * i + 2], v[4 * i + 3] * s[4 * i + 3]);
-    w[i] = a | (b << 16);
-  }
-}
 
 // Four E4M3 codes of the pairs a = (v0, v1), b = (v2, v3), each scaled by s.
 __device__ __forceinline__ uint32_t e4m3x4_pairs(uint64_t a, uint64_t b, uint64_t s) {
@@ -377,17 +357,9 @@ __device__ __forceinline__ float warp_max_nan(float v) {
   return v;
 }
 
-// Block-wide sum; every thread gets the same bits.  `buf` holds 32 floats and
-// must alternate between two buffers on consecutive calls (one barrier per
-// call suffices then).
-__device__ __forceinline__ float block_sum(float v, float* buf, int lane, int warp, int nwarps) {
-  v = warp_sum(v);
-  if (nwarps == 1) return v;
-  if (lane == 0) buf[warp] = v;
-  __syncthreads();
-  float r = lane < nwarps ? buf[lane] : 0.f;
-  return warp_sum(r);
-}
+// Block-wide sum of a pair; every thread gets the same bits.  `buf` holds 32
+// pairs and must alternate between two buffers on consecutive calls (one
+// barrier per call suffices then).
 __device__ __forceinline__ float2 block_sum2(float2 v, float2* buf, int lane, int warp,
                                              int nwarps) {
   v = warp_sum2(v);
@@ -518,25 +490,6 @@ __device__ __forceinline__ void push_stat(float2* buf, uint64_t* bar, uint32_t r
                : "memory");
 }
 
-// Reads a float2 from the shared memory of CTA `rank` of this cluster at the
-// address that `local` has in this CTA.
-__device__ __forceinline__ float2 dsmem_ld2(const float2* local, uint32_t rank) {
-  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
-  uint32_t ra;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
-  float2 v;
-  asm volatile("ld.shared::cluster.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(ra)
-               : "memory");
-  return v;
-}
 
-__device__ __forceinline__ int dsmem_ld_int(const int* local, uint32_t rank) {
-  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
-  uint32_t ra;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
-  int v;
-  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(ra) : "memory");
-  return v;
-}
 
 }  // namespace gbn

@@ -113,3 +113,24 @@ def test_bwd_validation_without_gpu(G):
 def test_bwd_workspace_query_without_device_reports_cuda_error(G):
     st, _ = G.gbn_norm_bwd_workspace_size(64, 1024, G.GBN_BF16, G.GBN_BF16, G.GBN_RMSNORM, 0, 0)
     assert st == G.GBN_ERR_CUDA
+
+
+def test_header_compiles_as_c99_and_cpp17(tmp_path):
+    import shutil
+    import subprocess
+    cuda_inc = "/usr/local/cuda/include"
+    if not shutil.which("gcc") or not os.path.exists(os.path.join(cuda_inc, "cuda_runtime_api.h")):
+        pytest.skip("gcc or the CUDA headers are not available")
+    src = tmp_path / "use.c"
+    src.write_text('#include "gbnorm.h"\n'
+                   "int main(void) {\n"
+                   "  gbn_quantize_layout l = (gbn_quantize_layout)(GBN_LAYOUT_ROWWISE |\n"
+                   "                                                GBN_LAYOUT_SWIZZLED_SCALES);\n"
+                   "  (void)l; (void)&gbn_norm_fwd; (void)&gbn_softmax_fwd;\n"
+                   "  return 0;\n}\n")
+    inc = ["-I", os.path.join(ROOT, "include"), "-I", cuda_inc]
+    for cmd in (["gcc", "-std=c99", "-Wall", "-Werror", "-fsyntax-only", *inc, str(src)],
+                ["g++", "-std=c++17", "-Wall", "-Werror", "-fsyntax-only", "-x", "c++", *inc,
+                 str(src)]):
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
