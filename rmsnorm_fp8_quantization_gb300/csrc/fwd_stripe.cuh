@@ -20,16 +20,20 @@
 //      bytes complete a transaction count on the receiver's mbarrier.  Every
 //      CTA merges the C partials of a row in rank order (identical results in
 //      all CTAs); no cluster-wide barrier per stripe.
-//   3. A thread item is 4 adjacent columns x all 32 rows, computed in packed
-//      fp32 pairs.  Delayed scaling: rowwise codes go to HBM as 4-byte words
-//      (a warp writes 128 contiguous bytes of a row); the codes are transposed
-//      in registers (4x4 byte transposes) and each column's 32 codes leave as
-//      one 32-byte store, a whole sector.  MXFP8: each 32x1 column block lies
-//      inside one thread (a pass for the column amax, a pass for the codes);
-//      the rowwise 1x32 blocks are done before, by warps walking rows in
-//      16-byte vectors (a block is 32/VEC adjacent lanes).
+//   3. Delayed scaling: a thread item is 4 adjacent columns x all 32 rows,
+//      computed in packed fp32 pairs.  Rowwise codes go to HBM as 4-byte
+//      words (a warp writes 128 contiguous bytes of a row); the codes are
+//      transposed in registers (4x4 byte transposes) and each column's 32
+//      codes leave as one 32-byte store, a whole sector.  MXFP8: a warp owns
+//      a band of 16 16-byte vectors over the 32 rows, a lane one vector of
+//      every other row.  A pass writes the rowwise codes (a 1x32 block is
+//      32/VEC adjacent lanes) and keeps each column's amax; a second pass,
+//      after one shuffle per column with the lane holding the other rows,
+//      writes the colwise codes.
 // x is read from HBM once.
 #pragma once
+
+#include <type_traits>
 
 #include "ring.cuh"
 
@@ -63,6 +67,31 @@ __device__ __forceinline__ void transpose4x4(const uint32_t* in, uint32_t* out) 
   out[3] = __byte_perm(t1, t3, 0x7632);
 }
 
+// x - mu (LayerNorm, neg_mu = -mu) or x (RMSNorm) of a 16-byte vector as
+// VEC/2 fp32 pairs.
+template <typename Tin, bool LN>
+__device__ __forceinline__ void centered_pairs(const uint4& u, float neg_mu, uint64_t* z) {
+  constexpr int VEC = 16 / (int)sizeof(Tin);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  widen_pairs<Tin, VEC>(w, z);
+  if constexpr (LN) {
+    const uint64_t c2 = p2(neg_mu, neg_mu);
+#pragma unroll
+    for (int i = 0; i < VEC / 2; ++i) z[i] = add2(z[i], c2);
+  }
+}
+
+// Code and multiplier 2^(127 - code) of the MX block scale for block amax
+// A >= 0 (or NaN): the code is A's exponent field minus 8 (the largest
+// exponent of E4M3), clamped at 0; Inf/NaN give code 255 and a NaN
+// multiplier.
+__device__ __forceinline__ void e8m0_scale(float A, uint32_t& code, float& mult) {
+  const uint32_t e = __float_as_uint(A) >> 23;
+  const uint32_t t = max(e, 8u);
+  code = e == 255u ? 255u : t - 8u;
+  mult = e == 255u ? __uint_as_float(0x7FFFFFFFu) : __uint_as_float((262u - t) << 23);
+}
+
 template <typename Tin, int QM, bool LN>
 __global__ void __launch_bounds__(kStripeThreads, 3)
     fwd_stripe_kernel(const FwdParams p, const int hc, const int stages) {
@@ -73,7 +102,10 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
   __shared__ uint64_t statbar[2];                       // all C stat pushes landed
   __shared__ float2 rbuf[2][kMaxCluster][kStripeRows];  // [stripe parity][sender][row]
   __shared__ float2 mystat[kStripeRows];
-  __shared__ float2 rstat[kStripeRows];                 // (mean, rsigma) per row
+  // per row: delayed scaling (mean, rsigma); MXFP8 (-mean, -mean, rsigma, rsigma),
+  // whose halves load as ready fp32 pairs
+  using RowStat = typename std::conditional<QM == Q_MXFP8, float4, float2>::type;
+  __shared__ RowStat rstat[kStripeRows];
   __shared__ float red[32];
   __shared__ int s_abort;
   __shared__ long long s_kfail;  // first stripe whose copy never landed
@@ -208,7 +240,10 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
         qsum += LN ? fmaf(fhc * d, d, v.y) : v.y;
       }
       const float rs = rsqrtf(fmaf(qsum, inv_h, p.eps));
-      rstat[r] = make_float2(mu, rs);
+      if constexpr (QM == Q_MXFP8)
+        rstat[r] = make_float4(-mu, -mu, rs, rs);
+      else
+        rstat[r] = make_float2(mu, rs);
       if (rank == 0) {
         if (LN && p.mu) p.mu[i0 + r] = mu;
         if (p.rsigma) p.rsigma[i0 + r] = rs;
@@ -221,119 +256,167 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
     // A 1x32 row block is 32/VEC adjacent lanes (shuffles); a 32x1 column
     // block is one lane's 16 rows plus its partner lane^16's.  Pass 1 writes
     // the rowwise codes and keeps the column amax; pass 2 the colwise codes.
+    // Each step takes two rows (r, r + 2) for independent work in flight.
     if constexpr (QM == Q_MXFP8) {
-      constexpr int NPV = VEC / 2;
-      constexpr int TPB = 32 / VEC;
-      const int vl = lane & 15, rp = lane >> 4;
-      const int nbands = nvs / 16;
-      const int64_t sc_stride = H / 32;
-      for (int band = warp; band < nbands; band += kStripeWarps) {
-        const int v = band * 16 + vl;
-        const int col = c0 + v * VEC;
-        uint64_t gw[NPV], bw[NPV];
+      auto bands = [&](auto rw_tag, auto swz_tag) {
+        constexpr bool RW = decltype(rw_tag)::value, SWZ = decltype(swz_tag)::value;
+        constexpr int NPV = VEC / 2;
+        constexpr int TPB = 32 / VEC;
+        const int vl = lane & 15, rp = lane >> 4;
+        const int nbands = nvs / 16;
+        const int64_t sc_stride = H / 32;
+        for (int band = warp; band < nbands; band += kStripeWarps) {
+          const int v = band * 16 + vl;
+          const int col = c0 + v * VEC;
+          uint64_t gw[NPV], bw[NPV];
 #pragma unroll
-        for (int h = 0; h < NPV / 2; ++h) {
-          const float4 g = reinterpret_cast<const float4*>(wg + v * VEC)[h];
-          gw[2 * h] = p2(g.x, g.y);
-          gw[2 * h + 1] = p2(g.z, g.w);
-          if constexpr (LN) {
-            const float4 bv = reinterpret_cast<const float4*>(wb + v * VEC)[h];
-            bw[2 * h] = p2(bv.x, bv.y);
-            bw[2 * h + 1] = p2(bv.z, bv.w);
-          } else {
-            bw[2 * h] = bw[2 * h + 1] = 0ull;
-          }
-        }
-        const uint4* xv = reinterpret_cast<const uint4*>(xs + rp * hc) + v;
-        const int xstep = 2 * nvs;  // vectors between rows r and r + 2
-        // z of the lane's vector in row r, as NPV pairs, with weights g, b
-        auto zvec = [&](int r, const uint64_t* g, const uint64_t* bb, uint64_t* z) {
-          const float2 st = rstat[r];
-          const uint64_t m2 = p2(st.x, st.x), r2 = p2(st.y, st.y);
-          const uint4 u = xv[(r >> 1) * xstep];
-          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-          widen_pairs<Tin, VEC>(w, z);
-#pragma unroll
-          for (int i = 0; i < NPV; ++i) {
-            const uint64_t t = mul2(LN ? sub2(z[i], m2) : z[i], r2);
-            z[i] = LN ? fma2(t, g[i], bb[i]) : mul2(t, g[i]);
-          }
-        };
-        float cm[VEC];
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) cm[e] = 0.f;
-        uint8_t* orow = p.write_rowwise ? reinterpret_cast<uint8_t*>(p.out) + (i0 + rp) * H + col
-                                        : nullptr;
-        int64_t srow = mx_row_scale_at(p, i0 + rp, col / 32);
-#pragma unroll 2
-        for (int r = rp; r < kStripeRows; r += 2) {
-          uint64_t z[NPV];
-          zvec(r, gw, bw, z);
-          float a = 0.f;
-#pragma unroll
-          for (int i = 0; i < NPV; ++i) {
-            const float2 f = u2(z[i]);
-            cm[2 * i] = fmax_nan(cm[2 * i], fabsf(f.x));
-            cm[2 * i + 1] = fmax_nan(cm[2 * i + 1], fabsf(f.y));
-            a = fmax_nan(a, fmax_nan(fabsf(f.x), fabsf(f.y)));
-          }
-          if (p.write_rowwise) {
-#pragma unroll
-            for (int o = 1; o < TPB; o <<= 1) a = fmax_nan(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
-            const uint32_t code = e8m0_code(a);
-            const float m = e8m0_mult(code);
-            const uint64_t s2 = p2(m, m);
-            uint32_t q[VEC / 4];
-#pragma unroll
-            for (int i = 0; i < VEC / 4; ++i) q[i] = e4m3x4_pairs(z[2 * i], z[2 * i + 1], s2);
-            st_words<VEC / 4>(orow, q);
-            if ((v & (TPB - 1)) == 0) p.mx_scale[srow] = static_cast<uint8_t>(code);
-            orow += 2 * H;
-            srow = p.mx_swizzle ? mx_row_scale_at(p, i0 + r + 2, col / 32) : srow + 2 * sc_stride;
-          }
-        }
-        if (p.write_colwise) {
-          uint32_t cw[VEC / 4];
-          uint64_t gm[NPV], bm[NPV];
-#pragma unroll
-          for (int i = 0; i < NPV; ++i) {
-            const float c0a = fmax_nan(cm[2 * i], __shfl_xor_sync(0xFFFFFFFFu, cm[2 * i], 16));
-            const float c1a = fmax_nan(cm[2 * i + 1], __shfl_xor_sync(0xFFFFFFFFu, cm[2 * i + 1], 16));
-            const uint32_t k0 = e8m0_code(c0a), k1 = e8m0_code(c1a);
-            if ((i & 1) == 0) cw[i / 2] = 0u;
-            cw[i / 2] |= (k0 | (k1 << 8)) << (16 * (i & 1));
-            // A power-of-two multiplier commutes exactly with the roundings
-            // of (x - mu) * rs * g' + beta (while g' and beta times it stay
-            // normal), so it is applied to g' and beta once.
-            const uint64_t m01 = p2(e8m0_mult(k0), e8m0_mult(k1));
-            gm[i] = mul2(gw[i], m01);
-            bm[i] = mul2(bw[i], m01);
-          }
-          if (rp == 0) {
-            if (p.mx_swizzle) {
-#pragma unroll
-              for (int e = 0; e < VEC; ++e)
-                p.mx_colwise_scale[mx_col_scale_at(p, stripe_of(k), col + e)] =
-                    static_cast<uint8_t>(cw[e / 4] >> (8 * (e & 3)));
+          for (int h = 0; h < NPV / 2; ++h) {
+            const float4 g = reinterpret_cast<const float4*>(wg + v * VEC)[h];
+            gw[2 * h] = p2(g.x, g.y);
+            gw[2 * h + 1] = p2(g.z, g.w);
+            if constexpr (LN) {
+              const float4 bv = reinterpret_cast<const float4*>(wb + v * VEC)[h];
+              bw[2 * h] = p2(bv.x, bv.y);
+              bw[2 * h + 1] = p2(bv.z, bv.w);
             } else {
-              st_words<VEC / 4>(p.mx_colwise_scale + stripe_of(k) * H + col, cw);
+              bw[2 * h] = bw[2 * h + 1] = 0ull;
             }
           }
-          uint8_t* crow = p.colwise_out + (i0 + rp) * H + col;
-#pragma unroll 2
-          for (int r = rp; r < kStripeRows; r += 2) {
-            uint64_t z[NPV];
-            zvec(r, gm, bm, z);
-            uint32_t q[VEC / 4];
-#pragma unroll
-            for (int i = 0; i < VEC / 4; ++i) {
-              const float2 fa = u2(z[2 * i]), fb = u2(z[2 * i + 1]);
-              q[i] = e4m3x2(fa.x, fa.y) | (e4m3x2(fb.x, fb.y) << 16);
+          const uint4* xv = reinterpret_cast<const uint4*>(xs + rp * hc) + v;
+          const int xstep = 2 * nvs;  // vectors between rows r and r + 2
+          // z of the lane's vector in row r, as NPV pairs, with weights g, b
+          auto zvec = [&](int r, const uint64_t* g, const uint64_t* bb, uint64_t* z) {
+            float neg_mu = 0.f;
+            uint64_t r2;
+            if constexpr (LN) {
+              const float4 st = rstat[r];
+              neg_mu = st.x;
+              r2 = p2(st.z, st.w);
+            } else {
+              const float2 st = reinterpret_cast<const float2*>(&rstat[r])[1];
+              r2 = p2(st.x, st.y);
             }
-            st_words<VEC / 4>(crow, q);
-            crow += 2 * H;
+            centered_pairs<Tin, LN>(xv[(r >> 1) * xstep], neg_mu, z);
+#pragma unroll
+            for (int i = 0; i < NPV; ++i) {
+              const uint64_t t = mul2(z[i], r2);
+              z[i] = LN ? fma2(t, g[i], bb[i]) : mul2(t, g[i]);
+            }
+          };
+          float cm[VEC];
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) cm[e] = 0.f;
+          uint8_t* orow = RW ? reinterpret_cast<uint8_t*>(p.out) + (i0 + rp) * H + col : nullptr;
+          int64_t srow = RW && !SWZ ? (i0 + rp) * sc_stride + col / 32 : 0;
+          const bool sc_lane = (v & (TPB - 1)) == 0;
+#pragma unroll 2
+          for (int r = rp; r < kStripeRows; r += 4) {
+            uint64_t za[NPV], zb[NPV];
+            zvec(r, gw, bw, za);
+            zvec(r + 2, gw, bw, zb);
+            float aa = 0.f, ab = 0.f;
+#pragma unroll
+            for (int i = 0; i < NPV; ++i) {
+              const float2 fa = u2(za[i]), fb = u2(zb[i]);
+              cm[2 * i] = fmax_nan(cm[2 * i], fmax_nan(fabsf(fa.x), fabsf(fb.x)));
+              cm[2 * i + 1] = fmax_nan(cm[2 * i + 1], fmax_nan(fabsf(fa.y), fabsf(fb.y)));
+              aa = fmax_nan(aa, fmax_nan(fabsf(fa.x), fabsf(fa.y)));
+              ab = fmax_nan(ab, fmax_nan(fabsf(fb.x), fabsf(fb.y)));
+            }
+            if constexpr (RW) {
+#pragma unroll
+              for (int o = 1; o < TPB; o <<= 1) {
+                aa = fmax_nan(aa, __shfl_xor_sync(0xFFFFFFFFu, aa, o));
+                ab = fmax_nan(ab, __shfl_xor_sync(0xFFFFFFFFu, ab, o));
+              }
+              uint32_t ka, kb;
+              float ma, mb;
+              e8m0_scale(aa, ka, ma);
+              e8m0_scale(ab, kb, mb);
+              const uint64_t sa = p2(ma, ma), sb = p2(mb, mb);
+              uint32_t qa[VEC / 4], qb[VEC / 4];
+#pragma unroll
+              for (int i = 0; i < VEC / 4; ++i) {
+                qa[i] = e4m3x4_pairs(za[2 * i], za[2 * i + 1], sa);
+                qb[i] = e4m3x4_pairs(zb[2 * i], zb[2 * i + 1], sb);
+              }
+              st_words<VEC / 4>(orow, qa);
+              st_words<VEC / 4>(orow + 2 * H, qb);
+              if (sc_lane) {
+                if constexpr (SWZ) {
+                  p.mx_scale[mx_row_scale_at(p, i0 + r, col / 32)] = static_cast<uint8_t>(ka);
+                  p.mx_scale[mx_row_scale_at(p, i0 + r + 2, col / 32)] = static_cast<uint8_t>(kb);
+                } else {
+                  p.mx_scale[srow] = static_cast<uint8_t>(ka);
+                  p.mx_scale[srow + 2 * sc_stride] = static_cast<uint8_t>(kb);
+                }
+              }
+              orow += 4 * H;
+              srow += 4 * sc_stride;
+            }
+          }
+          if (p.write_colwise) {
+            uint32_t cw[VEC / 4];
+            uint64_t gm[NPV], bm[NPV];
+#pragma unroll
+            for (int i = 0; i < NPV; ++i) {
+              const float c0a = fmax_nan(cm[2 * i], __shfl_xor_sync(0xFFFFFFFFu, cm[2 * i], 16));
+              const float c1a =
+                  fmax_nan(cm[2 * i + 1], __shfl_xor_sync(0xFFFFFFFFu, cm[2 * i + 1], 16));
+              uint32_t k0, k1;
+              float m0, m1;
+              e8m0_scale(c0a, k0, m0);
+              e8m0_scale(c1a, k1, m1);
+              if ((i & 1) == 0) cw[i / 2] = 0u;
+              cw[i / 2] |= (k0 | (k1 << 8)) << (16 * (i & 1));
+              // A power-of-two multiplier commutes exactly with the roundings
+              // of (x - mu) * rs * g' + beta (while g' and beta times it stay
+              // normal), so it is applied to g' and beta once.
+              const uint64_t m01 = p2(m0, m1);
+              gm[i] = mul2(gw[i], m01);
+              bm[i] = mul2(bw[i], m01);
+            }
+            if (rp == 0) {
+              if constexpr (SWZ) {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e)
+                  p.mx_colwise_scale[mx_col_scale_at(p, stripe_of(k), col + e)] =
+                      static_cast<uint8_t>(cw[e / 4] >> (8 * (e & 3)));
+              } else {
+                st_words<VEC / 4>(p.mx_colwise_scale + stripe_of(k) * H + col, cw);
+              }
+            }
+            uint8_t* crow = p.colwise_out + (i0 + rp) * H + col;
+#pragma unroll 2
+            for (int r = rp; r < kStripeRows; r += 4) {
+              uint64_t za[NPV], zb[NPV];
+              zvec(r, gm, bm, za);
+              zvec(r + 2, gm, bm, zb);
+              uint32_t qa[VEC / 4], qb[VEC / 4];
+#pragma unroll
+              for (int i = 0; i < VEC / 4; ++i) {
+                const float2 fa = u2(za[2 * i]), fb = u2(za[2 * i + 1]);
+                qa[i] = e4m3x2(fa.x, fa.y) | (e4m3x2(fb.x, fb.y) << 16);
+                const float2 ga = u2(zb[2 * i]), gb = u2(zb[2 * i + 1]);
+                qb[i] = e4m3x2(ga.x, ga.y) | (e4m3x2(gb.x, gb.y) << 16);
+              }
+              st_words<VEC / 4>(crow, qa);
+              st_words<VEC / 4>(crow + 2 * H, qb);
+              crow += 4 * H;
+            }
           }
         }
+      };
+      if (p.write_rowwise) {
+        if (p.mx_swizzle)
+          bands(std::true_type{}, std::true_type{});
+        else
+          bands(std::true_type{}, std::false_type{});
+      } else {
+        if (p.mx_swizzle)
+          bands(std::false_type{}, std::true_type{});
+        else
+          bands(std::false_type{}, std::false_type{});
       }
     }
 
