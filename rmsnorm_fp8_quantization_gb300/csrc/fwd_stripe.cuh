@@ -182,42 +182,60 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
     wait(&full[b], par, k);
     const Tin* xs = reinterpret_cast<const Tin*>(xbuf + b * slice);
 
-    // ---- 1. slice statistics, warp w owns rows 4w .. 4w+3
-    constexpr int NP = VEC / 2;
+    // ---- 1. slice statistics, warp w owns rows 4w .. 4w+3; the four rows
+    // are walked together (independent loads and shuffles in flight).
+    {
+      constexpr int NP = VEC / 2;
+      constexpr int RW4 = kRowsPerWarp;
+      const uint4* xr = reinterpret_cast<const uint4*>(xs + warp * RW4 * hc);
+      float m[RW4];
 #pragma unroll
-    for (int rr = 0; rr < kRowsPerWarp; ++rr) {
-      const int r = warp * kRowsPerWarp + rr;
-      const uint4* xr = reinterpret_cast<const uint4*>(xs + r * hc);
-      float m = 0.f;
+      for (int rr = 0; rr < RW4; ++rr) m[rr] = 0.f;
       if constexpr (LN) {
-        uint64_t a = 0ull;
+        uint64_t a[RW4];
+#pragma unroll
+        for (int rr = 0; rr < RW4; ++rr) a[rr] = 0ull;
         for (int v = lane; v < nvs; v += 32) {
-          const uint4 u = xr[v];
+#pragma unroll
+          for (int rr = 0; rr < RW4; ++rr) {
+            const uint4 u = xr[rr * nvs + v];
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+            uint64_t pr[NP];
+            widen_pairs<Tin, VEC>(w, pr);
+#pragma unroll
+            for (int i = 0; i < NP; ++i) a[rr] = add2(a[rr], pr[i]);
+          }
+        }
+#pragma unroll
+        for (int rr = 0; rr < RW4; ++rr) {
+          const float2 af = u2(a[rr]);
+          m[rr] = warp_sum(af.x + af.y) / fhc;
+        }
+      }
+      uint64_t q2[RW4];
+#pragma unroll
+      for (int rr = 0; rr < RW4; ++rr) q2[rr] = 0ull;
+      for (int v = lane; v < nvs; v += 32) {
+#pragma unroll
+        for (int rr = 0; rr < RW4; ++rr) {
+          const uint4 u = xr[rr * nvs + v];
           const uint32_t w[4] = {u.x, u.y, u.z, u.w};
           uint64_t pr[NP];
           widen_pairs<Tin, VEC>(w, pr);
+          const uint64_t m2 = p2(m[rr], m[rr]);
 #pragma unroll
-          for (int i = 0; i < NP; ++i) a = add2(a, pr[i]);
-        }
-        const float2 af = u2(a);
-        m = warp_sum(af.x + af.y) / fhc;
-      }
-      const uint64_t m2 = p2(m, m);
-      uint64_t q2 = 0ull;
-      for (int v = lane; v < nvs; v += 32) {
-        const uint4 u = xr[v];
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-        uint64_t pr[NP];
-        widen_pairs<Tin, VEC>(w, pr);
-#pragma unroll
-        for (int i = 0; i < NP; ++i) {
-          const uint64_t d = LN ? sub2(pr[i], m2) : pr[i];
-          q2 = fma2(d, d, q2);
+          for (int i = 0; i < NP; ++i) {
+            const uint64_t d = LN ? sub2(pr[i], m2) : pr[i];
+            q2[rr] = fma2(d, d, q2[rr]);
+          }
         }
       }
-      const float2 qf = u2(q2);
-      const float q = warp_sum(qf.x + qf.y);
-      if (lane == 0) mystat[r] = make_float2(m, q);
+#pragma unroll
+      for (int rr = 0; rr < RW4; ++rr) {
+        const float2 qf = u2(q2[rr]);
+        const float q = warp_sum(qf.x + qf.y);
+        if (lane == 0) mystat[warp * RW4 + rr] = make_float2(m[rr], q);
+      }
     }
     __syncthreads();
     if (warp == 0) {
