@@ -398,36 +398,97 @@ def copy_calibration(dev):
 
 
 def run_e2e(ops, w, inp, args, barrier, world, dev):
-    """Same step through the C ABI with host buffers: H2D of x, dz, gamma,
-    beta from pinned memory, forward, backward, D2H of out, mu, rsigma, dx,
-    dgamma, dbeta, all inside the timed region."""
-    host_in = {k: inp[k].cpu().pin_memory() for k in ("x", "dz", "gamma", "beta")}
-    dev_in = {k: torch.empty_like(inp[k]) for k in host_in}
-    dinp = dict(inp)
-    dinp.update(dev_in)
-    fwd, bwd, outs, (dx, dg, db) = make_step(ops, w, dinp)
-    res = [outs["out"], outs["mu"], outs["rsigma"], dx, dg, db]
-    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in res]
+    """Same step through the C ABI with host buffers: every step copies x,
+    dz, gamma, beta host -> device from pinned memory, runs the forward and
+    the backward, and copies out, mu, rsigma, dx, dgamma, dbeta device ->
+    host, all inside the timed region.
 
-    def h2d():
-        for k in host_in:
-            dev_in[k].copy_(host_in[k], non_blocking=True)
+    Headline: two buffer sets and three streams (copies in, compute, copies
+    out), so step i's device -> host copies overlap step i+1's host -> device
+    copies and kernels, as a pipeline feeding the GPU would run.  `serial`
+    is the same work on one stream, nothing overlapped."""
+    keys = ("x", "dz", "gamma", "beta")
+    host_in = {k: inp[k].cpu().pin_memory() for k in keys}
+    sets = []
+    for _ in range(2):
+        dev_in = {k: torch.empty_like(inp[k]) for k in keys}
+        dinp = dict(inp)
+        dinp.update(dev_in)
+        fwd, bwd, outs, (dx, dg, db) = make_step(ops, w, dinp)
+        res = [outs["out"], outs["mu"], outs["rsigma"], dx, dg, db]
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in res]
+        sets.append((dev_in, fwd, bwd, res, host_out))
+    h2d_bytes = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h_bytes = sum(t.numel() * t.element_size() for t in sets[0][4])
+    steps = max(3, args.steps // 2)
 
-    def d2h():
-        for h, d in zip(host_out, res):
+    def h2d(b):
+        for k in keys:
+            sets[b][0][k].copy_(host_in[k], non_blocking=True)
+
+    def d2h(b):
+        for h, d in zip(sets[b][4], sets[b][3]):
             h.copy_(d, non_blocking=True)
 
-    steps = max(3, args.steps // 2)
-    _, tot = time_calls([h2d, fwd, bwd, d2h], steps, args.warmup, None, barrier)
+    # serial: one stream, one buffer set
+    _, tot_serial = time_calls([lambda: h2d(0), sets[0][1], sets[0][2], lambda: d2h(0)], steps,
+                               args.warmup, None, barrier)
+
+    # pipelined
+    cur = torch.cuda.current_stream()
+    s_in, s_c, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    in_ready, in_free, out_ready, out_free = ([ev(), ev()] for _ in range(4))
+    for e in in_free + out_free:
+        e.record(cur)
+
+    def step(i):
+        b = i % 2
+        s_in.wait_event(in_free[b])
+        with torch.cuda.stream(s_in):
+            h2d(b)
+        in_ready[b].record(s_in)
+        s_c.wait_event(in_ready[b])
+        s_c.wait_event(out_free[b])
+        with torch.cuda.stream(s_c):
+            sets[b][1]()
+            sets[b][2]()
+        in_free[b].record(s_c)
+        out_ready[b].record(s_c)
+        s_out.wait_event(out_ready[b])
+        with torch.cuda.stream(s_out):
+            d2h(b)
+        out_free[b].record(s_out)
+
+    def run(n):
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(cur)
+        s_in.wait_event(start)
+        for i in range(n):
+            step(i)
+        cur.wait_stream(s_out)
+        end.record(cur)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end)
+
+    run(max(args.warmup, 2))
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    tot = run(steps)
     if world > 1:
         import torch.distributed as dist
-        t = torch.tensor([tot], device=dev)
+        t = torch.tensor([tot, tot_serial], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot = float(t.item())
+        tot, tot_serial = float(t[0].item()), float(t[1].item())
     return {"value": w.rows * steps * world / (tot / 1e3), "unit": "rows/s",
-            "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host_in.values()),
-            "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out),
-            "ms_per_step": tot / steps}
+            "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
+            "ms_per_step": tot / steps,
+            "pipeline": "2 buffer sets; host->device copies, kernels and device->host copies "
+                        "on three streams (step i's copies out overlap step i+1's copies in)",
+            "serial": {"value": w.rows * steps * world / (tot_serial / 1e3),
+                       "ms_per_step": tot_serial / steps}}
 
 
 def run_detail(ops, WORKLOADS, make_inputs, args, flush, dev, peak):
