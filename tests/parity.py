@@ -6,7 +6,8 @@ result meaningless):
   * fp32 results: |got - ref| <= 1e-5 |ref| + 8 * 2^-24 * T
   * bf16 / f16 results: |got - ref| <= 1 ulp(ref) + 8 * 2^-24 * T
     where T is the magnitude of the terms the kernel adds in fp32
-    (for z: |x - mu| rsigma |g'| + |beta|; for dx: rsigma (|dy| +
+    (for z: |x - mu| rsigma |g'| + |beta|, plus mean|x| rsigma |g'| for
+    LayerNorm, the summands of mu standing for its fp32 error; for dx: rsigma (|dy| +
     mean|dy| + |xhat| mean|dy xhat|) + |dresidual|, the summands of c1 =
     mean(dy) and c2 = mean(dy xhat) standing for their fp32 error).
   * mu / rsigma: rel 1e-4 (plus the same fp32 term bound for mu).
@@ -112,10 +113,16 @@ def check_scales(name, got, ref, block_amax):
 # ---------------------------------------------------------------- expected values
 
 def z_terms(x, gamma, beta, mu, rs, norm, zcg):
-    """|x - mu| rsigma |g'| + |beta| per element (magnitude of the fp32 terms of z)."""
+    """Magnitude of the fp32 terms of z per element: |x - mu| rsigma |g'| +
+    |beta|, and for LayerNorm mean_j |x_j| rsigma |g'| -- the kernel's mu is
+    an fp32 sum of the row, whose evaluation error scales with its summands,
+    not with |x - mu| (an element close to the mean would otherwise get no
+    room for it)."""
     xd = to64(x) if not isinstance(x, np.ndarray) else x
     g = to64(gamma) + (1.0 if zcg else 0.0)
     t = np.abs(xd - (mu[:, None] if norm == 0 else 0.0)) * rs[:, None] * np.abs(g)[None, :]
+    if norm == 0:
+        t = t + np.abs(xd).mean(axis=1, keepdims=True) * rs[:, None] * np.abs(g)[None, :]
     if beta is not None and norm == 0:
         t = t + np.abs(to64(beta))[None, :]
     return t
