@@ -11,8 +11,11 @@
 // warps, one to eight), each holding NV loads of V elements in registers, so a
 // row is read once and written once.  The reductions (max, then sum; or
 // sum dy * y) run over the group: warp shuffles, then shared memory when
-// WPR > 1.  exp is taken as exp2f of x * scale * log2(e) less its row
-// maximum.
+// WPR > 1.  exp is taken as 2^(x * scale * log2(e) - (max - 64)): the
+// hardware ex2 (flush-to-zero) on arguments at most 64, whose results stay
+// normal for every term above 2^-190; the common factor 2^64 cancels in the
+// normalization, and the final multiply by 1/sum (in full fp32, subnormal
+// results included) rounds each output once from its normal-range term.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -28,6 +31,13 @@ namespace {
 constexpr int kSmThreads = 256;
 constexpr int64_t kMaxSoftmaxKeys = GBN_SOFTMAX_MAX_KEYS;
 constexpr float kLog2e = 1.4426950408889634f;
+
+// 2^a by the hardware approximation, subnormal results flushed to zero.
+__device__ __forceinline__ float ex2_ftz(float a) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(a));
+  return r;
+}
 
 template <typename T>
 struct SmElem;
@@ -211,22 +221,29 @@ __global__ void __launch_bounds__(kSmThreads, NV == 8 ? 2 : 4)
     for (int k = 0; k < NV; ++k) {
       const int j0 = (k * gthreads + t) * V;
       words_to_floats<T, V>(w[k], u[k]);
+      if (MASK != 1 && j0 + V <= limit) {  // the whole vector is kept
 #pragma unroll
-      for (int e = 0; e < V; ++e) {
-        bool keep = j0 + e < limit;
-        if constexpr (MASK == 1) keep = keep && ((mb[k] >> (8 * e)) & 0xFFu) == 0;
-        u[k][e] = keep ? u[k][e] * p.scale_log2e : -INFINITY;
-        m = fmaxf(m, u[k][e]);
+        for (int e = 0; e < V; ++e) u[k][e] *= p.scale_log2e;
+      } else {
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+          bool keep = j0 + e < limit;
+          if constexpr (MASK == 1) keep = keep && ((mb[k] >> (8 * e)) & 0xFFu) == 0;
+          u[k][e] = keep ? u[k][e] * p.scale_log2e : -INFINITY;
+        }
       }
+#pragma unroll
+      for (int e = 0; e < V; ++e) m = fmaxf(m, u[k][e]);
     }
     m = group_reduce<true>(m, buf, p.wpr);
-    const float mo = m == -INFINITY ? 0.f : m;  // nothing kept: every term is exp2(-inf) = 0
+    // nothing kept: every term is 2^-inf = 0
+    const float mo = (m == -INFINITY ? 0.f : m) - 64.f;
     float s = 0.f;
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
 #pragma unroll
       for (int e = 0; e < V; ++e) {
-        u[k][e] = exp2f(u[k][e] - mo);
+        u[k][e] = ex2_ftz(u[k][e] - mo);
         s += u[k][e];
       }
     }
