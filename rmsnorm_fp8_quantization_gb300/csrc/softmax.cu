@@ -223,17 +223,21 @@ __global__ void __launch_bounds__(kSmThreads, NV == 8 ? 2 : 4)
       words_to_floats<T, V>(w[k], u[k]);
       if (MASK != 1 && j0 + V <= limit) {  // the whole vector is kept
 #pragma unroll
-        for (int e = 0; e < V; ++e) u[k][e] *= p.scale_log2e;
+        for (int e = 0; e < V; ++e) {
+          u[k][e] *= p.scale_log2e;
+          m = fmaxf(m, u[k][e]);
+        }
+      } else if (MASK != 1 && j0 >= limit) {
+        // nothing of this vector is kept: no part in the max or the sum
       } else {
 #pragma unroll
         for (int e = 0; e < V; ++e) {
           bool keep = j0 + e < limit;
           if constexpr (MASK == 1) keep = keep && ((mb[k] >> (8 * e)) & 0xFFu) == 0;
           u[k][e] = keep ? u[k][e] * p.scale_log2e : -INFINITY;
+          m = fmaxf(m, u[k][e]);
         }
       }
-#pragma unroll
-      for (int e = 0; e < V; ++e) m = fmaxf(m, u[k][e]);
     }
     m = group_reduce<true>(m, buf, p.wpr);
     // nothing kept: every term is 2^-inf = 0
@@ -241,10 +245,16 @@ __global__ void __launch_bounds__(kSmThreads, NV == 8 ? 2 : 4)
     float s = 0.f;
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
+      const int j0 = (k * gthreads + t) * V;
+      if (MASK != 1 && j0 >= limit) {
 #pragma unroll
-      for (int e = 0; e < V; ++e) {
-        u[k][e] = ex2_ftz(u[k][e] - mo);
-        s += u[k][e];
+        for (int e = 0; e < V; ++e) u[k][e] = 0.f;
+      } else {
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+          u[k][e] = ex2_ftz(u[k][e] - mo);
+          s += u[k][e];
+        }
       }
     }
     s = group_reduce<false>(s, buf, p.wpr);
