@@ -236,8 +236,8 @@ __global__ void __launch_bounds__(fwd_ring_max_threads(NV))
           constexpr int TPB = 32 / VEC;
 #pragma unroll
           for (int o2 = 1; o2 < TPB; o2 <<= 1) a = fmax_nan(a, __shfl_xor_sync(0xFFFFFFFFu, a, o2));
-          code = e8m0_code(a);
-          const float m = e8m0_mult(code);
+          float m;
+          e8m0_scale(a, code, m);
           s2 = p2(m, m);
         }
         if (act) {

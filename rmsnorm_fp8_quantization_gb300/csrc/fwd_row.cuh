@@ -77,8 +77,9 @@ __global__ void __launch_bounds__(256) fwd_generic_kernel(const FwdParams p) {
           float a = 0.f;
           for (int e = 0; e < 32; ++e)
             a = fmax_nan(a, fabsf(z_at<Tin>(p, row, blk * 32 + e, s_mean[r], s_rs[r], gadd, ln)));
-          const uint32_t c = e8m0_code(a);
-          const float m = e8m0_mult(c);
+          uint32_t c;
+          float m;
+          e8m0_scale(a, c, m);
           uint8_t* o = reinterpret_cast<uint8_t*>(p.out) + row * H + blk * 32;
           for (int e = 0; e < 32; ++e)
             o[e] = e4m3(z_at<Tin>(p, row, blk * 32 + e, s_mean[r], s_rs[r], gadd, ln) * m);
@@ -115,8 +116,9 @@ __global__ void __launch_bounds__(256) fwd_generic_kernel(const FwdParams p) {
           float a = 0.f;
           for (int r = 0; r < 32; ++r)
             a = fmax_nan(a, fabsf(z_at<Tin>(p, i0 + r, j, s_mean[r], s_rs[r], gadd, ln)));
-          const uint32_t c = e8m0_code(a);
-          const float m = e8m0_mult(c);
+          uint32_t c;
+          float m;
+          e8m0_scale(a, c, m);
           for (int r = 0; r < 32; ++r)
             p.colwise_out[(i0 + r) * H + j] =
                 e4m3(z_at<Tin>(p, i0 + r, j, s_mean[r], s_rs[r], gadd, ln) * m);

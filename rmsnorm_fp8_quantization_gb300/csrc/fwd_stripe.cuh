@@ -81,17 +81,6 @@ __device__ __forceinline__ void centered_pairs(const uint4& u, float neg_mu, uin
   }
 }
 
-// Code and multiplier 2^(127 - code) of the MX block scale for block amax
-// A >= 0 (or NaN): the code is A's exponent field minus 8 (the largest
-// exponent of E4M3), clamped at 0; Inf/NaN give code 255 and a NaN
-// multiplier.
-__device__ __forceinline__ void e8m0_scale(float A, uint32_t& code, float& mult) {
-  const uint32_t e = __float_as_uint(A) >> 23;
-  const uint32_t t = max(e, 8u);
-  code = e == 255u ? 255u : t - 8u;
-  mult = e == 255u ? __uint_as_float(0x7FFFFFFFu) : __uint_as_float((262u - t) << 23);
-}
-
 template <typename Tin, int QM, bool LN>
 __global__ void __launch_bounds__(kStripeThreads, 3)
     fwd_stripe_kernel(const FwdParams p, const int hc, const int stages) {

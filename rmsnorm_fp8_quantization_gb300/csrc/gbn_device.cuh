@@ -301,19 +301,17 @@ __device__ __forceinline__ float fmax_nan(float a, float b) {
   return r;
 }
 
-// E8M0 code of the MX block scale for block amax A >= 0 (or NaN): the biased
-// exponent of 2^(floor(log2 A) - 8), 8 being the largest exponent of E4M3.
-// floor(log2 A) + 127 is A's exponent field for normal A; zero and subnormal
-// A clamp to code 0; Inf/NaN give 255.
-__device__ __forceinline__ uint32_t e8m0_code(float A) {
+// Code and multiplier of the MX block scale for block amax A >= 0 (or NaN):
+// the code is the biased exponent of 2^(floor(log2 A) - 8), 8 being the
+// largest exponent of E4M3 -- A's exponent field minus 8 for normal A,
+// clamped at 0 (zero and subnormal A give 0); Inf/NaN give code 255.  The
+// multiplier is 2^(127 - code) as fp32 (always normal: code <= 246 for
+// finite A), NaN for code 255.
+__device__ __forceinline__ void e8m0_scale(float A, uint32_t& code, float& mult) {
   const uint32_t e = __float_as_uint(A) >> 23;  // sign is 0 for A >= 0
-  if (e >= 255u) return 255u;
-  return e > 8u ? e - 8u : 0u;
-}
-// 2^(127 - code) as fp32 (code <= 246 for finite fp32 A, so always normal);
-// NaN for code 255.
-__device__ __forceinline__ float e8m0_mult(uint32_t code) {
-  return code == 255u ? __uint_as_float(0x7FFFFFFFu) : __uint_as_float((254u - code) << 23);
+  const uint32_t t = max(e, 8u);
+  code = e == 255u ? 255u : t - 8u;
+  mult = e == 255u ? __uint_as_float(0x7FFFFFFFu) : __uint_as_float((262u - t) << 23);
 }
 
 // Byte offset of scale (r, c) in the tiled GEMM order: 512-byte tiles of
