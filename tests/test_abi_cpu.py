@@ -68,6 +68,8 @@ def test_fwd_validation_without_gpu(G):
     assert _fwd(G, in_dtype=G.GBN_E4M3) == G.GBN_ERR_DTYPE
     assert _fwd(G, hidden=0) == G.GBN_ERR_SHAPE
     assert _fwd(G, rows=-1) == G.GBN_ERR_SHAPE
+    assert _fwd(G, hidden=(1 << 24) + 1) == G.GBN_ERR_SHAPE                 # past the largest row
+    assert _fwd(G, hidden=1 << 24) == G.GBN_ERR_NULL                         # the largest passes shape
     mx = dict(scaling_mode=G.GBN_SCALING_MXFP8_1D, out_dtype=G.GBN_E4M3)
     assert _fwd(G, hidden=48, **mx) == G.GBN_ERR_SHAPE                       # blocks of 32
     assert _fwd(G, rows=40, quantize_layout=G.GBN_LAYOUT_COLWISE, **mx) == G.GBN_ERR_SHAPE
@@ -104,6 +106,8 @@ def test_bwd_validation_without_gpu(G):
     assert _bwd(G, norm_type=2, **ok) == G.GBN_ERR_ENUM
     assert _bwd(G, w_dtype=G.GBN_E8M0, **ok) == G.GBN_ERR_DTYPE
     assert _bwd(G, hidden=0, **ok) == G.GBN_ERR_SHAPE
+    assert _bwd(G, hidden=(1 << 24) + 1, **ok) == G.GBN_ERR_SHAPE
+    assert _bwd(G, rows=-1, **ok) == G.GBN_ERR_SHAPE
     assert _bwd(G, norm_type=G.GBN_LAYERNORM, **ok) == G.GBN_ERR_NULL       # mu, dbeta
     assert _bwd(G, **ok) == G.GBN_ERR_WORKSPACE                             # no workspace
     assert _bwd(G, workspace=FAKE + 4, **ok) == G.GBN_ERR_WORKSPACE         # misaligned

@@ -29,6 +29,13 @@ FWD = [
     ("mxfp8 rowwise 49152", wl("rms_bf16_mxfp8_16384x5120", 32, 49152, layout="rowwise")),
     ("ln mxfp8 rowwise 36864", wl("rms_bf16_mxfp8_16384x5120", 24, 36864, layout="rowwise",
                                   norm="layernorm")),
+    # the longest rows the clusters take (8 CTAs x 16384 two-byte / 8192 four-byte elements)
+    ("ln 131072 longest cluster row", wl("ln_bf16_16384x4096", 9, 131072)),
+    ("rms f32 65536 longest cluster row", wl("rms_f32_64x1024", 7, 65536)),
+    # one vector past them: the generic kernel
+    ("ln 131080 generic", wl("ln_bf16_16384x4096", 5, 131080)),
+    ("delayed rowwise 139264 generic", wl("rms_bf16_e4m3_delayed_32768x8192", 4, 139264,
+                                           layout="rowwise")),
 ]
 
 
@@ -43,6 +50,11 @@ BWD = [
     ("ln add f16 ragged 20000", wl("ln_bf16_16384x4096", 19, 20000, in_dtype="f16",
                                     w_dtype="f16", dresidual=True)),
     ("rms f32 12288", wl("rms_f32_64x1024", 20, 12288)),
+    # the longest backward rows the clusters take, and one vector past them (generic kernel)
+    ("ln f16 65536 longest cluster row", wl("ln_bf16_16384x4096", 9, 65536, in_dtype="f16",
+                                            w_dtype="f16")),
+    ("rms add 65544 generic", wl("rms_bwd_add_bf16_32768x12288", 5, 65544)),
+    ("ln f32 32772 generic", wl("rms_f32_64x1024", 6, 32772, norm="layernorm")),
 ]
 
 
