@@ -22,6 +22,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -606,7 +607,23 @@ def cpu_baseline(args, min_seconds=10.0):
             break
     return {"value": w.rows * reps / el, "unit": "rows/s", "cores": 1, "kind": "oracle",
             "sample": f"full {w.rows}x{w.hidden} LayerNorm fwd+bwd, {reps} repetitions, "
-                      f"{el:.1f} s, single-threaded C++ (double)"}
+                      f"{el:.1f} s, single-threaded C++ (double)",
+            "host": host_description()}
+
+
+def host_description():
+    """The host the CPU legs ran on: logical CPUs and the CPU model string."""
+    model = platform.machine()
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":", 1)[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return {"nproc": os.cpu_count(), "cpu": model, "arch": platform.machine()}
 
 
 def run_reference(args):
@@ -646,7 +663,8 @@ def run_reference(args):
         "config": {"workload": MAIN, "rows": w.rows, "hidden": w.hidden,
                    "sample_rows_per_step": sample.rows},
         "cpu_baseline": {"value": v, "unit": "rows/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{sample.rows} rows of {MAIN} per step (fwd+bwd)"},
+                         "sample": f"{sample.rows} rows of {MAIN} per step (fwd+bwd)",
+                         "host": host_description()},
         "e2e": {"value": v, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
 
