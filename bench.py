@@ -378,6 +378,7 @@ def run_gpu(args):
     }
     if rank == 0:
         result["cpu_baseline"] = cpu_baseline(args)
+        result["cpu_baseline_all_cores"] = cpu_baseline_all_cores()
         print(json.dumps(result))
     if dist:
         dist.barrier()
@@ -608,6 +609,55 @@ def cpu_baseline(args, min_seconds=10.0):
     return {"value": w.rows * reps / el, "unit": "rows/s", "cores": 1, "kind": "oracle",
             "sample": f"full {w.rows}x{w.hidden} LayerNorm fwd+bwd, {reps} repetitions, "
                       f"{el:.1f} s, single-threaded C++ (double)",
+            "host": host_description()}
+
+
+def cpu_baseline_all_cores(min_seconds=10.0):
+    """The same oracle with the rows split over every host core: one thread
+    per core runs the oracle's C functions on a contiguous slice of the rows
+    (the foreign calls release the interpreter lock), and the slices'
+    dgamma / dbeta are added afterwards.  Labelled apart from the
+    single-threaded baseline; the oracle itself is unchanged."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import numpy as np
+
+    import oracle
+    from rmsnorm_fp8_quantization_gb300.workloads import WORKLOADS, make_inputs
+    w = WORKLOADS[MAIN]
+    inp = make_inputs(w, seed=0)
+    oracle.build()
+    n = max(1, os.cpu_count() or 1)
+    bounds = np.linspace(0, w.rows, n + 1).astype(int)
+
+    def part(i):
+        sl = slice(int(bounds[i]), int(bounds[i + 1]))
+        z, mu, rs = oracle.norm_fwd(inp["x"][sl], inp["gamma"], inp["beta"], 0, False, w.eps)
+        oracle.round_to(z, "bf16")
+        del z
+        dx, dg, db = oracle.norm_bwd(inp["dz"][sl], inp["x"][sl], mu.astype(np.float32),
+                                     rs.astype(np.float32), inp["gamma"], None, 0, False)
+        oracle.round_to(dx, "bf16")
+        return dg, db
+
+    part(0)  # loads the oracle library before the threads start
+    reps = 0
+    with ThreadPoolExecutor(max_workers=n) as ex:
+        t0 = time.perf_counter()
+        while True:
+            parts = list(ex.map(part, range(n)))
+            dg = sum(p[0] for p in parts)
+            db = sum(p[1] for p in parts)
+            oracle.round_to(dg, "f32")
+            oracle.round_to(db, "f32")
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= min_seconds or reps >= 50:
+                break
+    return {"value": w.rows * reps / el, "unit": "rows/s", "cores": n,
+            "kind": "oracle, rows split over all host cores",
+            "sample": f"full {w.rows}x{w.hidden} LayerNorm fwd+bwd, {reps} repetitions, "
+                      f"{el:.1f} s, {n} threads",
             "host": host_description()}
 
 
