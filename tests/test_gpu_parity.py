@@ -8,8 +8,8 @@ import pytest
 import torch
 
 import oracle
-from parity import (block_amax_colwise, block_amax_rowwise, bwd_terms, check_codes, check_float,
-                    check_scales, z_terms)
+from parity import (amax_f32, block_amax_colwise, block_amax_rowwise, bwd_terms, check_codes,
+                    check_float, check_scales, check_wgrad, kernel_z32, same_f32_bits, z_terms)
 from rmsnorm_fp8_quantization_gb300.workloads import WORKLOADS, Workload, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -52,6 +52,7 @@ def run_fwd_and_check(ops, w: Workload, seed=0, sm_margin=0, inputs=None):
             if rowwise:
                 assert torch.equal(out["colwise_out"].T, out["out"]), "colwise is not the transpose"
         check_float("amax", out["updated_amax"], np.array([amax]), torch.float32, rel=1e-5)
+        check_amax_bits(out, inp, w)
     else:
         if rowwise:
             q, s = oracle.mxfp8_rowwise(z)
@@ -64,6 +65,19 @@ def run_fwd_and_check(ops, w: Workload, seed=0, sm_margin=0, inputs=None):
             same = np.repeat(out["colwise_scale_inv"].cpu().numpy() == s, 32, axis=0)
             check_codes("colwise_out", out["colwise_out"], q, mask=same)
     return out, inp, (z, mu, rs)
+
+
+def check_amax_bits(out, inp, w):
+    """The updated amax is max|z| of the kernel's own fp32 z, bit for bit:
+    z recomputed in fp32 from the statistics the kernel saved, in the
+    kernel's order of operations (``kernel_z32``)."""
+    norm = NORM[w.norm]
+    z32 = kernel_z32(inp["x"], inp["gamma"], inp["beta"],
+                     out["mu"].cpu().numpy() if norm == 0 else None, out["rsigma"].cpu().numpy(),
+                     norm, w.zero_centered_gamma)
+    want = amax_f32(z32)
+    got = np.float32(out["updated_amax"].item())
+    assert same_f32_bits(got, want), f"amax {got!r} is not max|z| of the kernel's z {want!r}"
 
 
 def run_bwd_and_check(ops, w: Workload, seed=0, sm_margin=0, inputs=None):
@@ -84,12 +98,9 @@ def run_bwd_and_check(ops, w: Workload, seed=0, sm_margin=0, inputs=None):
                                  w.zero_centered_gamma)
     wdt = DT[w.w_dtype]
     check_float("dx", dx, rdx, DT[w.in_dtype], terms=t_dx)
-    k = 1e-6 / 2.0 ** -24
-    check_float("dgamma", dg, rdg, wdt, terms=t_dg, k=k,
-                rel=1e-4 if wdt == torch.float32 else None)
+    check_wgrad("dgamma", dg, rdg, wdt, t_dg)
     if norm == 0:
-        check_float("dbeta", db, rdb, wdt, terms=t_db, k=k,
-                    rel=1e-4 if wdt == torch.float32 else None)
+        check_wgrad("dbeta", db, rdb, wdt, t_db)
     return dx, dg, db
 
 

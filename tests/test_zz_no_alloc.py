@@ -1,20 +1,19 @@
-"""gbn_norm_bwd_noalloc: the workspace-free backward, for callers that cannot
-allocate device memory, must give the same results as gbn_norm_bwd with a
-caller-provided workspace.
+"""gbn_norm_bwd_noalloc, the backward for callers that cannot allocate device
+memory at the point where they run it (a framework replaying a fixed memory
+plan, a plugin host without an allocator, a caller inside a custom
+allocator's own callback): it must give exactly what gbn_norm_bwd gives with
+a caller-provided workspace, because it runs the same kernels on the same
+grid with the partial sums in the library's own scratch array instead.
 
 Collected last (file name) so that a run that stops at the first failure has
 already run every other test; it also passes alone in a fresh process.
 """
-import numpy as np
 import pytest
 import torch
 
-from parity import bwd_terms, check_float
 from rmsnorm_fp8_quantization_gb300.workloads import WORKLOADS, make_inputs
 
 pytestmark = pytest.mark.gpu
-
-DT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
 
 
 def _noalloc(G, dz, x, mu, rs, gamma, dres, dx, dg, db, norm, zcg):
@@ -25,6 +24,23 @@ def _noalloc(G, dz, x, mu, rs, gamma, dres, dx, dg, db, norm, zcg):
                                   zcg, 0)
 
 
+def _problem(name, rows, hidden, seed):
+    w = WORKLOADS[name].with_shape(rows, hidden)
+    inp = make_inputs(w, seed=seed)
+    c = lambda t: None if t is None else t.cuda()
+    ln = w.norm == "layernorm"
+    g = torch.Generator().manual_seed(seed)
+    rs = (torch.rand(rows, generator=g) + 0.5).cuda()
+    mu = (torch.randn(rows, generator=g) * 0.1).cuda() if ln else None
+    return w, c(inp["dz"]), c(inp["x"]), mu, rs, c(inp["gamma"]), c(inp["dresidual"])
+
+
+def _outputs(x, gamma, ln):
+    nan = float("nan")
+    return (torch.full_like(x, nan), torch.full_like(gamma, nan),
+            torch.full_like(gamma, nan) if ln else None)
+
+
 @pytest.mark.parametrize("name,rows,hidden", [
     ("ln_bf16_16384x4096", 300, 4096),
     ("rms_bwd_add_bf16_32768x12288", 257, 12288),
@@ -32,41 +48,41 @@ def _noalloc(G, dz, x, mu, rs, gamma, dres, dx, dg, db, norm, zcg):
 ])
 def test_noalloc_matches_workspace_backward(gpu, name, rows, hidden):
     from rmsnorm_fp8_quantization_gb300 import gbnorm as G
-    w = WORKLOADS[name].with_shape(rows, hidden)
-    inp = make_inputs(w, seed=3)
-    c = lambda t: None if t is None else t.cuda()
-    x, dz, gamma, dres = c(inp["x"]), c(inp["dz"]), c(inp["gamma"]), c(inp["dresidual"])
+    w, dz, x, mu, rs, gamma, dres = _problem(name, rows, hidden, seed=3)
     ln = w.norm == "layernorm"
-    rs = torch.rand(rows, device="cuda") + 0.5
-    mu = (torch.randn(rows, device="cuda") * 0.1) if ln else None
-    ref = gpu.norm_bwd(dz, x, mu, rs, gamma, dres, norm=w.norm)
+    # Reference: the allocating entry point with a NaN-filled workspace, so a
+    # partial row the kernels failed to write would show.
+    ws = gpu.bwd_workspace(rows, hidden, x.dtype, gamma.dtype, w.norm).fill_(0xFF)
+    ref = gpu.norm_bwd(dz, x, mu, rs, gamma, dres, norm=w.norm, workspace=ws)
     torch.cuda.synchronize()
-    for _ in range(2):   # two calls in a row share (and must fully rewrite) the scratch
-        dx = torch.full_like(x, float("nan"))
-        dg = torch.full_like(gamma, float("nan"))
-        db = torch.full_like(gamma, float("nan")) if ln else None
+    # Another problem that fills more of the scratch, with other values.
+    w2, *other = _problem("ln_bf16_16384x4096", 2000, 8192, seed=11)
+    for call in range(2):
+        if call == 1:
+            o2 = _outputs(other[1], other[4], True)
+            st = _noalloc(G, *other, *o2, "layernorm", False)
+            assert st == G.GBN_OK, G.gbn_status_string(st)
+        dx, dg, db = _outputs(x, gamma, ln)
         st = _noalloc(G, dz, x, mu, rs, gamma, dres, dx, dg, db, w.norm, False)
         assert st == G.GBN_OK, G.gbn_status_string(st)
         torch.cuda.synchronize()
-        t_dx, t_dg, t_db = bwd_terms(dz, x, None if mu is None else mu.cpu().numpy(),
-                                     rs.cpu().numpy(), gamma, dres, 0 if ln else 1, False)
-        k = 1e-6 / 2.0 ** -24
-        check_float("dx", dx, ref[0].double().cpu().numpy(), DT[w.in_dtype], terms=t_dx)
-        check_float("dgamma", dg, ref[1].double().cpu().numpy(), DT[w.w_dtype], terms=t_dg, k=k,
-                    rel=1e-4 if DT[w.w_dtype] == torch.float32 else None)
+        assert torch.equal(dx, ref[0]), f"call {call}: dx differs"
+        assert torch.equal(dg, ref[1]), f"call {call}: dgamma differs"
         if ln:
-            check_float("dbeta", db, ref[2].double().cpu().numpy(), DT[w.w_dtype], terms=t_db,
-                        k=k, rel=1e-4 if DT[w.w_dtype] == torch.float32 else None)
+            assert torch.equal(db, ref[2]), f"call {call}: dbeta differs"
 
 
 def test_noalloc_rejects_oversized_problem(gpu):
     from rmsnorm_fp8_quantization_gb300 import gbnorm as G
     # partial rows of (SMs x CTAs per SM) x hidden fp32 do not fit the scratch
-    hidden = 1 << 22
-    st, need = G.gbn_norm_bwd_workspace_size(1 << 20, hidden, G.GBN_BF16, G.GBN_BF16,
+    rows, hidden = 1 << 20, 1 << 22
+    st, need = G.gbn_norm_bwd_workspace_size(rows, hidden, G.GBN_BF16, G.GBN_BF16,
                                              G.GBN_LAYERNORM, 0, 0)
     assert st == G.GBN_OK and need > (32 << 20)
-    fake = 256  # never dereferenced: the size check fails before any launch
-    st = G.gbn_norm_bwd_noalloc(fake, fake, fake, fake, fake, None, fake, fake, fake, 1 << 20,
-                                hidden, G.GBN_BF16, G.GBN_BF16, G.GBN_LAYERNORM, 0, 0, stream=0)
+    # Row-sized buffers are NULL: were the size check ever moved after the
+    # argument checks, the call would return GBN_ERR_NULL, never launch.
+    gamma = torch.ones(8, dtype=torch.bfloat16, device="cuda")
+    dg, db = torch.empty_like(gamma), torch.empty_like(gamma)
+    st = G.gbn_norm_bwd_noalloc(None, None, None, None, gamma, None, None, dg, db, rows, hidden,
+                                G.GBN_BF16, G.GBN_BF16, G.GBN_LAYERNORM, 0, 0, stream=0)
     assert st == G.GBN_ERR_WORKSPACE
