@@ -10,8 +10,8 @@ the elements that are within tolerance only because of that extra term, and
 the tests bound and report the count.
 
   * fp32 results: |got - ref| <= 1e-5 |ref| + k * 2^-24 * T
-  * bf16 / f16 results: |got - ref| <= 1 ulp(ref) + k * 2^-24 * T, k = 8,
-    where T is the magnitude of the terms the kernel adds in fp32
+  * bf16 / f16 results: |got - ref| <= 1 ulp(ref) + k * 2^-24 * T,
+    k = 8, where T is the magnitude of the terms the kernel adds in fp32
     (for z: |x - mu| rsigma |g'| + |beta|, plus mean|x| rsigma |g'| for
     LayerNorm, the summands of mu standing for its fp32 error; for dx: rsigma (|dy| +
     mean|dy| + |xhat| mean|dy xhat|) + |dresidual|, the summands of c1 =
@@ -21,15 +21,15 @@ the tests bound and report the count.
   * The counts of elements relying on the fp32 term are bounded by 0.1% of
     the elements (z, dx, mu) or 2% (dgamma / dbeta, whose exact value is a
     sum over all rows that often nearly cancels), plus two elements.
-  * dgamma / dbeta: rel 1e-4 plus 1e-6 * sum_i |term_i| (fp32 partial sums
-    over all rows; far below one row's contribution, so a dropped or doubled
-    row still fails).  bf16 weights: 1 bf16 ulp plus the same.
+  * dgamma / dbeta: rel 1e-4 plus 1e-6 * sum_i |term_i| (fp32 partial
+    sums over all rows; far below one row's contribution, so a dropped or
+    doubled row still fails).  bf16 weights: 1 bf16 ulp plus the same.
   * E4M3 codes: within 1 step everywhere, at most 0.1% of codes differ.
-  * E8M0 scales: bit-exact except blocks whose amax lies within 4 fp32 ulp of
-    a power of two (counted, bounded).
-  * amax (delayed scaling): bit-exact against max|z| of the kernel's own fp32
-    z (``kernel_z32``, from the kernel's saved statistics), rel 1e-5 against
-    the oracle.
+  * E8M0 scales: bit-exact except blocks whose amax lies within 4 fp32
+    ulp of a power of two (counted, bounded).
+  * amax, delayed scaling: bit-exact against max|z| of the kernel's own
+    fp32 z (``kernel_z32``, from the kernel's saved statistics), rel 1e-5
+    against the oracle.
 
 Set GBN_PARITY_REPORT to a file path to have every count appended there as
 one JSON line per check.
