@@ -58,8 +58,9 @@ int fwd_ring_cap(int nv) { return fwd_ring_max_threads(nv); }
 int bwd_threads_cap(int nv) { return bwd_max_threads(nv); }
 
 // Cluster split of a 32-row stripe for the columnwise layouts.  Candidates:
-// C <= 8 CTAs per cluster, each taking hc = hidden / C columns (a multiple of
-// 8 and of the 16-byte vector; of 128 for MXFP8), at most 2048 two-byte or
+// C <= 16 CTAs per cluster (above 8 as a non-portable cluster size), each
+// taking hc = hidden / C columns (a multiple of 8 and of the 16-byte vector;
+// of 128 for MXFP8), at most 2048 two-byte or
 // 1024 four-byte columns, with the slice (or two, when they fit) in shared
 // memory.  Among them the one with the most co-resident CTAs (clusters x C;
 // packing differs per C, and small slices fit several CTAs per SM), weighted
@@ -85,13 +86,13 @@ bool stripe_geom(const KernelTable& kt, int in, int qm, bool ln, int64_t hidden,
   bool found = false;
   StripeGeom best{};
   int best_active = -1;
-  for (int c = 1; c <= 8; ++c) {
+  for (int c = 1; c <= 16; ++c) {
     if (hidden % c) continue;
     const int64_t hc = hidden / c;
     // 16-byte vectors; MXFP8 in whole bands of 16 vectors (hc % 128 for 2- and 4-byte inputs).
     if (hc % vec || hc % 8 || (qm == Q_MXFP8 && hc % 128) || hc > hc_max) continue;
     for (int stages = 2; stages >= 1; --stages) {
-      const int smem = stripe_smem_bytes(qm, ln, static_cast<int>(hc), esize, stages);
+      const int smem = stripe_smem_bytes(qm, ln, static_cast<int>(hc), esize, stages, c);
       if (smem > kMaxSmemPerCta) continue;
       StripeGeom g{c, static_cast<int>(hc), stages, smem, 0};
       int n = 0;

@@ -30,6 +30,8 @@
 //      32/VEC adjacent lanes) and keeps each column's amax; a second pass,
 //      after one shuffle per column with the lane holding the other rows,
 //      writes the colwise codes.
+//   Slice rows sit 16 bytes apart beyond their length in shared memory, so
+//   that the lanes of a tile, reading 8 rows at once, hit distinct banks.
 // x is read from HBM once.
 #pragma once
 
@@ -41,7 +43,7 @@ namespace gbn {
 
 constexpr int kStripeWarps = kStripeThreads / 32;
 constexpr int kRowsPerWarp = kStripeRows / kStripeWarps;  // 4
-constexpr int kMaxCluster = 8;
+constexpr int kMaxCluster = 16;
 
 // Four consecutive elements of a shared-memory row as two fp32 pairs.
 template <typename Tin>
@@ -89,7 +91,6 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint64_t full[2];                          // x slice landed
   __shared__ uint64_t statbar[2];                       // all C stat pushes landed
-  __shared__ float2 rbuf[2][kMaxCluster][kStripeRows];  // [stripe parity][sender][row]
   __shared__ float2 mystat[kStripeRows];
   // per row: delayed scaling (mean, rsigma); MXFP8 (-mean, -mean, rsigma, rsigma),
   // whose halves load as ready fp32 pairs
@@ -112,11 +113,17 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
   const int64_t count = cid < nstripes ? (nstripes - 1 - cid) / ncl + 1 : 0;
   const float inv_h = 1.f / static_cast<float>(H), fhc = static_cast<float>(hc);
   const uint32_t row_bytes = static_cast<uint32_t>(hc) * sizeof(Tin);
-  const uint32_t slice = kStripeRows * row_bytes;
+  const uint32_t rstride = row_bytes + 16;  // shared-memory bytes between slice rows
+  const uint32_t slice = kStripeRows * rstride;
   const Tin* x = reinterpret_cast<const Tin*>(p.x);
   uint8_t* xbuf = smem;
-  float* wg = reinterpret_cast<float*>(smem + stages * slice);  // g' [hc]
-  float* wb = wg + hc;                                          // beta [hc] (LayerNorm)
+  // statistics pushed by the cluster's CTAs: [stripe parity][sender][row]
+  float2* rbuf = reinterpret_cast<float2*>(smem + stages * slice);
+  float* wg = reinterpret_cast<float*>(rbuf + 2 * C * kStripeRows);  // g' [hc]
+  float* wb = wg + hc;                                              // beta [hc] (LayerNorm)
+  auto rb_at = [&](int par, uint32_t sender, int row) -> float2& {
+    return rbuf[(par * C + sender) * kStripeRows + row];
+  };
   float qscale = 1.f;
   if constexpr (QM == Q_DELAYED) qscale = *p.scale;
   float amax_t = 0.f;
@@ -124,9 +131,9 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
   auto stripe_of = [&](int64_t k) { return cid + k * ncl; };
   auto issue = [&](int b, int64_t k) {
     const int64_t i0 = stripe_of(k) * kStripeRows;
-    mbar_arrive_expect_tx(&full[b], slice);
+    mbar_arrive_expect_tx(&full[b], kStripeRows * row_bytes);
     for (int r = 0; r < kStripeRows; ++r)
-      bulk_g2s(xbuf + b * slice + r * row_bytes, x + (i0 + r) * H + c0, row_bytes, &full[b]);
+      bulk_g2s(xbuf + b * slice + r * rstride, x + (i0 + r) * H + c0, row_bytes, &full[b]);
   };
   // Bounded waits by one thread, the rest of the CTA blocked on the barrier
   // that follows (no spinning warps).  After the first timeout every later
@@ -169,14 +176,16 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
     const int sb = static_cast<int>(k & 1);  // stat buffer
     if (tid == 0) mbar_arrive_expect_tx(&statbar[sb], C * kStripeRows * sizeof(float2));
     wait(&full[b], par, k);
-    const Tin* xs = reinterpret_cast<const Tin*>(xbuf + b * slice);
+    const uint8_t* xsb = xbuf + b * slice;
+    const Tin* xs = reinterpret_cast<const Tin*>(xsb);
+    const int xrow = static_cast<int>(rstride / sizeof(Tin));  // elements between slice rows
 
     // ---- 1. slice statistics, warp w owns rows 4w .. 4w+3; the four rows
     // are walked together (independent loads and shuffles in flight).
     {
       constexpr int NP = VEC / 2;
       constexpr int RW4 = kRowsPerWarp;
-      const uint4* xr = reinterpret_cast<const uint4*>(xs + warp * RW4 * hc);
+      const uint8_t* xr = xsb + warp * RW4 * rstride;
       float m[RW4];
 #pragma unroll
       for (int rr = 0; rr < RW4; ++rr) m[rr] = 0.f;
@@ -187,7 +196,7 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
         for (int v = lane; v < nvs; v += 32) {
 #pragma unroll
           for (int rr = 0; rr < RW4; ++rr) {
-            const uint4 u = xr[rr * nvs + v];
+            const uint4 u = reinterpret_cast<const uint4*>(xr + rr * rstride)[v];
             const uint32_t w[4] = {u.x, u.y, u.z, u.w};
             uint64_t pr[NP];
             widen_pairs<Tin, VEC>(w, pr);
@@ -207,7 +216,7 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
       for (int v = lane; v < nvs; v += 32) {
 #pragma unroll
         for (int rr = 0; rr < RW4; ++rr) {
-          const uint4 u = xr[rr * nvs + v];
+          const uint4 u = reinterpret_cast<const uint4*>(xr + rr * rstride)[v];
           const uint32_t w[4] = {u.x, u.y, u.z, u.w};
           uint64_t pr[NP];
           widen_pairs<Tin, VEC>(w, pr);
@@ -228,7 +237,7 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
     }
     __syncthreads();
     if (warp == 0) {
-      for (uint32_t c = 0; c < C; ++c) push_stat(&rbuf[sb][rank][lane], &statbar[sb], c, mystat[lane]);
+      for (uint32_t c = 0; c < C; ++c) push_stat(&rb_at(sb, rank, lane), &statbar[sb], c, mystat[lane]);
     }
     wait(&statbar[sb], static_cast<uint32_t>((k >> 1) & 1), -1);
 
@@ -238,11 +247,11 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
       float mu = 0.f, qsum = 0.f;
       if constexpr (LN) {
         float msum = 0.f;
-        for (uint32_t c = 0; c < C; ++c) msum += rbuf[sb][c][r].x;
+        for (uint32_t c = 0; c < C; ++c) msum += rb_at(sb, c, r).x;
         mu = msum / static_cast<float>(C);
       }
       for (uint32_t c = 0; c < C; ++c) {
-        const float2 v = rbuf[sb][c][r];
+        const float2 v = rb_at(sb, c, r);
         const float d = v.x - mu;
         qsum += LN ? fmaf(fhc * d, d, v.y) : v.y;
       }
@@ -289,8 +298,8 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
               bw[2 * h] = bw[2 * h + 1] = 0ull;
             }
           }
-          const uint4* xv = reinterpret_cast<const uint4*>(xs + rp * hc) + v;
-          const int xstep = 2 * nvs;  // vectors between rows r and r + 2
+          const uint4* xv = reinterpret_cast<const uint4*>(xsb + rp * rstride) + v;
+          const int xstep = 2 * static_cast<int>(rstride / 16);  // vectors between rows r and r + 2
           // z of the lane's vector in row r, as NPV pairs, with weights g, b
           auto zvec = [&](int r, const uint64_t* g, const uint64_t* bb, uint64_t* z) {
             float neg_mu = 0.f;
@@ -446,7 +455,7 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
         const float2 st = rstat[r];
         const uint64_t m2 = p2(st.x, st.x), r2 = p2(st.y, st.y);
         uint64_t xp[2];
-        lds4_pairs<Tin>(xcol + r * hc, xp);
+        lds4_pairs<Tin>(xcol + r * xrow, xp);
         const uint64_t t01 = mul2(LN ? sub2(xp[0], m2) : xp[0], r2);
         const uint64_t t23 = mul2(LN ? sub2(xp[1], m2) : xp[1], r2);
         z01 = LN ? fma2(t01, ga, ba) : mul2(t01, ga);

@@ -119,11 +119,14 @@ __host__ __device__ constexpr int ring_slot_bytes(int nv, int threads) { return 
 constexpr int kStripeRows = 32;
 constexpr int kStripeThreads = 256;
 
-// Dynamic shared memory of the stripe kernel: `stages` x 32-row slices of x,
+// Dynamic shared memory of the stripe kernel: `stages` x 32-row slices of x
+// (rows 16 bytes apart beyond their length), the statistics pushed by the
+// cluster's CTAs (two stripes x `cluster` senders x 32 rows of float2),
 // then the CTA's weights (g' and, for LayerNorm, beta; fp32).
-inline int stripe_smem_bytes(int qm, bool ln, int hc, int esize, int stages) {
+inline int stripe_smem_bytes(int qm, bool ln, int hc, int esize, int stages, int cluster) {
   (void)qm;
-  return stages * kStripeRows * hc * esize + (ln ? 8 : 4) * hc;
+  return stages * kStripeRows * (hc * esize + 16) + 2 * cluster * kStripeRows * 8 +
+         (ln ? 8 : 4) * hc;
 }
 
 // Launchers of one input dtype (one translation unit each).  Every function

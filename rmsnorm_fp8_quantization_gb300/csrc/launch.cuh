@@ -67,9 +67,11 @@ struct Launch {
     if (!k) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
-    stripe_config(g, 1024 / g.cluster, &cfg, attr);
+    stripe_config(g, 960 / g.cluster, &cfg, attr);
     return cudaOccupancyMaxActiveClusters(n, k, &cfg);
   }
   static cudaError_t stripe_launch(int qm, bool ln, const StripeGeom& g, const FwdParams& p,
@@ -77,6 +79,8 @@ struct Launch {
     Kstripe3 k = stripe_kernel(qm, ln);
     if (!k) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
