@@ -387,19 +387,35 @@ def run_gpu(args):
 
 def copy_calibration(dev):
     """GB/s of torch's own elementwise kernels on this GPU, timed like the
-    main step (back to back): a bf16 copy (one read, one write stream) and a
-    bf16 multiply (two reads, one write) of 16384 x 4096.  Context for the
-    roofline fraction, not its denominator."""
+    main step (back to back, CUDA events, median): a bf16 copy (one read,
+    one write stream) at the workload's size (16384 x 4096: 2 x 134 MB) and
+    at 1 Gi elements (2 x 2 GiB, the size of the measured HBM peak), and a
+    bf16 multiply (two reads, one write) at the workload's size.  Context for
+    the roofline fraction -- what a plain streaming kernel reaches at each
+    size -- not its denominator."""
+    def gbs(fn, nbytes, steps):
+        per, _ = time_calls([fn], steps, 5)
+        return nbytes / (statistics.median(per[0]) / 1e3) / 1e9
+
+    out = {}
     a = torch.zeros(16384, 4096, dtype=torch.bfloat16, device=dev)
     b = torch.zeros_like(a)
     o = torch.empty_like(a)
     nb = a.numel() * a.element_size()
-    per_c, _ = time_calls([lambda: o.copy_(a)], 20, 5)
-    per_m, _ = time_calls([lambda: torch.mul(a, b, out=o)], 20, 5)
-    out = {"copy": 2 * nb / (statistics.median(per_c[0]) / 1e3) / 1e9,
-           "mul": 3 * nb / (statistics.median(per_m[0]) / 1e3) / 1e9}
+    out["copy_workload_size"] = gbs(lambda: o.copy_(a), 2 * nb, 20)
+    out["mul_workload_size"] = gbs(lambda: torch.mul(a, b, out=o), 3 * nb, 20)
     del a, b, o
     torch.cuda.empty_cache()
+    try:
+        a = torch.zeros(1 << 30, dtype=torch.bfloat16, device=dev)
+        o = torch.empty_like(a)
+        out["copy_2gib"] = gbs(lambda: o.copy_(a), 2 * a.numel() * a.element_size(), 10)
+        del a, o
+    except torch.cuda.OutOfMemoryError:
+        out["copy_2gib"] = None
+    torch.cuda.empty_cache()
+    out["sizes"] = {"workload": "2 x 134,217,728 bytes (copy), 3 x (mul)",
+                    "2gib": "2 x 2,147,483,648 bytes"}
     return out
 
 
@@ -522,6 +538,12 @@ def run_detail(ops, WORKLOADS, make_inputs, args, flush, dev, peak):
                       "gbs": gbs, "frac_of_peak": gbs / peak,
                       "frac_of_8tbs": gbs / NOMINAL_HBM_GBS,
                       "fits_in_l2": nb < L2_BYTES}
+            if nb < L2_BYTES:
+                # far below a microsecond of HBM time: the per-call latency
+                # (launch and one pass of the kernel) is the figure, and the
+                # workload is outside the bandwidth target
+                d[lab]["launch_bound"] = True
+                d[lab]["latency_us"] = ms * 1e3
         out[name] = d
         del inp, outs, grads, fwd, bwd
         torch.cuda.empty_cache()
