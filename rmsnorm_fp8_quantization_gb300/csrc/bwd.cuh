@@ -21,7 +21,7 @@ namespace gbn {
 template <typename Tin>
 __global__ void __launch_bounds__(256) bwd_generic_kernel(const BwdParams p) {
   pdl_begin();
-  __shared__ float2 red[2][32];
+  __shared__ __align__(16) float2 red[2][32];
   const int tid = threadIdx.x, T = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5, nwarps = T >> 5;
   const int H = p.hidden;
@@ -37,6 +37,8 @@ __global__ void __launch_bounds__(256) bwd_generic_kernel(const BwdParams p) {
     pg[j] = 0.f;
     if (ln) pb[j] = 0.f;
   }
+  // slots past the warp count read as zero in the block sums; no warp writes them
+  for (int i = nwarps + tid; i < 32; i += T) red[0][i] = red[1][i] = make_float2(0.f, 0.f);
   int rb = 0;
   for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
     const int64_t base = row * H;

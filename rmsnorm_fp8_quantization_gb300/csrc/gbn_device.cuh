@@ -356,14 +356,30 @@ __device__ __forceinline__ float warp_max_nan(float v) {
 }
 
 // Block-wide sum of a pair; every thread gets the same bits.  `buf` holds 32
-// pairs and must alternate between two buffers on consecutive calls (one
-// barrier per call suffices then).
+// pairs (16-byte aligned) and must alternate between two buffers on
+// consecutive calls (one barrier per call suffices then).  Up to 8 warps,
+// every thread reads the warp partials from shared memory and adds them in
+// one fixed tree order (entries at and past nwarps read as zero) instead of
+// a second shuffle tree.
 __device__ __forceinline__ float2 block_sum2(float2 v, float2* buf, int lane, int warp,
                                              int nwarps) {
   v = warp_sum2(v);
   if (nwarps == 1) return v;
   if (lane == 0) buf[warp] = v;
   __syncthreads();
+  if (nwarps <= 8) {
+    const float4* b4 = reinterpret_cast<const float4*>(buf);
+    const float4 a = b4[0];
+    const float4 b = nwarps > 2 ? b4[1] : make_float4(0.f, 0.f, 0.f, 0.f);
+    float2 r = make_float2((a.x + a.z) + (b.x + b.z), (a.y + a.w) + (b.y + b.w));
+    if (nwarps > 4) {
+      const float4 c = b4[2];
+      const float4 d = nwarps > 6 ? b4[3] : make_float4(0.f, 0.f, 0.f, 0.f);
+      r.x += (c.x + c.z) + (d.x + d.z);
+      r.y += (c.y + c.w) + (d.y + d.w);
+    }
+    return r;
+  }
   float2 r = lane < nwarps ? buf[lane] : make_float2(0.f, 0.f);
   return warp_sum2(r);
 }

@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(bwd_max_threads(NV)) bwd_ring_kernel(const Bwd
   constexpr bool KEEP = (NV == 1) || (NV == 2 && !LN);
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ uint64_t full[kMaxRingStages];
-  __shared__ float2 red[2][32];
+  __shared__ __align__(16) float2 red[2][32];
   __shared__ int s_abort;
   const int tid = threadIdx.x, T = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5, nwarps = T >> 5;
@@ -365,6 +365,8 @@ __global__ void __launch_bounds__(bwd_max_threads(NV)) bwd_ring_kernel(const Bwd
   }
   __syncthreads();
 
+  // slots past the warp count read as zero in the block sums; no warp writes them
+  for (int i = nwarps + tid; i < 32; i += T) red[0][i] = red[1][i] = make_float2(0.f, 0.f);
   int rb = 0;
   int st = 0;          // stage of row k
   uint32_t phase = 0;  // its mbarrier phase parity
