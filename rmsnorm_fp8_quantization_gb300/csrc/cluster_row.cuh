@@ -184,17 +184,26 @@ __global__ void __launch_bounds__(fwd_ring_max_threads(NV))
     // Merge in rank order (the same bits in every CTA of the cluster).
     const float2* e = ex.entries(k);
     float mean = 0.f, ss = 0.f;
+    // (unrolled to the largest cluster, entries past C skipped: no loop
+    // branches per row in every thread)
     if constexpr (LN) {
       float msum = 0.f;
-      for (uint32_t c = 0; c < C; ++c) msum += e[c].x;
+#pragma unroll
+      for (uint32_t c = 0; c < kMaxRowCluster; ++c)
+        if (c < C) msum += e[c].x;
       mean = msum / static_cast<float>(C);
       const float fhc = static_cast<float>(hc);
-      for (uint32_t c = 0; c < C; ++c) {
-        const float d = e[c].x - mean;
-        ss += fmaf(fhc * d, d, e[c].y);
+#pragma unroll
+      for (uint32_t c = 0; c < kMaxRowCluster; ++c) {
+        if (c < C) {
+          const float d = e[c].x - mean;
+          ss += fmaf(fhc * d, d, e[c].y);
+        }
       }
     } else {
-      for (uint32_t c = 0; c < C; ++c) ss += e[c].y;
+#pragma unroll
+      for (uint32_t c = 0; c < kMaxRowCluster; ++c)
+        if (c < C) ss += e[c].y;
     }
     const float rs = rsqrtf(fmaf(ss, inv_h, p.eps));
     const uint64_t rs2 = p2(rs, rs), mean2 = p2(mean, mean);
@@ -430,9 +439,12 @@ __global__ void __launch_bounds__(bwd_max_threads(NV))
     {
       const float2* e = ex.entries(k);
       float tx = 0.f, ty = 0.f;
-      for (uint32_t c = 0; c < C; ++c) {
-        tx += e[c].x;
-        ty += e[c].y;
+#pragma unroll
+      for (uint32_t c = 0; c < kMaxRowCluster; ++c) {
+        if (c < C) {
+          tx += e[c].x;
+          ty += e[c].y;
+        }
       }
       s = make_float2(tx, ty);
     }
