@@ -237,7 +237,10 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
     }
     __syncthreads();
     if (warp == 0) {
-      for (uint32_t c = 0; c < C; ++c) push_stat(&rb_at(sb, rank, lane), &statbar[sb], c, mystat[lane]);
+      const float2 mine = mystat[lane];
+#pragma unroll
+      for (uint32_t c = 0; c < kMaxCluster; ++c)
+        if (c < C) push_stat(&rb_at(sb, rank, lane), &statbar[sb], c, mine);
     }
     wait(&statbar[sb], static_cast<uint32_t>((k >> 1) & 1), -1);
 
@@ -245,15 +248,21 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
     if (warp == 0) {
       const int r = lane;
       float mu = 0.f, qsum = 0.f;
+      // (unrolled to the largest cluster, entries past C skipped)
       if constexpr (LN) {
         float msum = 0.f;
-        for (uint32_t c = 0; c < C; ++c) msum += rb_at(sb, c, r).x;
+#pragma unroll
+        for (uint32_t c = 0; c < kMaxCluster; ++c)
+          if (c < C) msum += rb_at(sb, c, r).x;
         mu = msum / static_cast<float>(C);
       }
-      for (uint32_t c = 0; c < C; ++c) {
-        const float2 v = rb_at(sb, c, r);
-        const float d = v.x - mu;
-        qsum += LN ? fmaf(fhc * d, d, v.y) : v.y;
+#pragma unroll
+      for (uint32_t c = 0; c < kMaxCluster; ++c) {
+        if (c < C) {
+          const float2 v = rb_at(sb, c, r);
+          const float d = v.x - mu;
+          qsum += LN ? fmaf(fhc * d, d, v.y) : v.y;
+        }
       }
       const float rs = rsqrtf(fmaf(qsum, inv_h, p.eps));
       if constexpr (QM == Q_MXFP8)
