@@ -367,13 +367,22 @@ __global__ void __launch_bounds__(bwd_max_threads(NV))
   const int64_t vstep = static_cast<int64_t>(T) * VEC;
   const float* mup = LN ? p.mu + cid : nullptr;
   const float* rsp = p.rsigma + cid;
-  for (; k < count; ++k, dxrow += row_step, rsp += ncl) {
+  // Row statistics are loaded one row ahead so their latency is hidden.
+  float mu_next = 0.f, rs_next = 0.f;
+  if (count > 0) {
+    if constexpr (LN) mu_next = *mup;
+    rs_next = *rsp;
+  }
+  for (; k < count; ++k, dxrow += row_step) {
     if (tid == 0) ex.arm(k);
-    const float rs = *rsp;
-    float mu = 0.f;
-    if constexpr (LN) {
-      mu = *mup;
-      mup += ncl;
+    const float rs = rs_next, mu = mu_next;
+    if (k + 1 < count) {
+      rsp += ncl;
+      rs_next = *rsp;
+      if constexpr (LN) {
+        mup += ncl;
+        mu_next = *mup;
+      }
     }
     if (!mbar_wait(&full[st], phase)) s_abort = 1;
     uint32_t dzw[NV][NW], xw[NV][NW], rw[ADD ? NV : 1][NW];

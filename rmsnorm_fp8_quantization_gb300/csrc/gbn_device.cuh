@@ -357,10 +357,10 @@ __device__ __forceinline__ float warp_max_nan(float v) {
 
 // Block-wide sum of a pair; every thread gets the same bits.  `buf` holds 32
 // pairs (16-byte aligned) and must alternate between two buffers on
-// consecutive calls (one barrier per call suffices then).  Up to 8 warps,
+// consecutive calls (one barrier per call suffices then).  Up to 16 warps,
 // every thread reads the warp partials from shared memory and adds them in
-// one fixed tree order (entries at and past nwarps read as zero) instead of
-// a second shuffle tree.
+// one fixed order (entries at and past nwarps read as zero) instead of a
+// second shuffle tree.
 __device__ __forceinline__ float2 block_sum2(float2 v, float2* buf, int lane, int warp,
                                              int nwarps) {
   v = warp_sum2(v);
@@ -377,6 +377,17 @@ __device__ __forceinline__ float2 block_sum2(float2 v, float2* buf, int lane, in
       const float4 d = nwarps > 6 ? b4[3] : make_float4(0.f, 0.f, 0.f, 0.f);
       r.x += (c.x + c.z) + (d.x + d.z);
       r.y += (c.y + c.w) + (d.y + d.w);
+    }
+    return r;
+  }
+  if (nwarps <= 16) {
+    const float4* b4 = reinterpret_cast<const float4*>(buf);
+    float2 r = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 a = b4[2 * q], b = b4[2 * q + 1];
+      r.x += (a.x + a.z) + (b.x + b.z);
+      r.y += (a.y + a.w) + (b.y + b.w);
     }
     return r;
   }
