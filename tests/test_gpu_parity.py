@@ -153,6 +153,10 @@ FWD_DELAYED_CASES = [
        layout="rowwise"),
     wl(DEL, rows=64, hidden=8192, norm="layernorm", w_dtype="bf16", beta_std=0.1,
        zero_centered_gamma=True, gamma_mean=0.0, gamma_std=0.05),
+    # rows a multiple of 16 but not of 32: the generic kernel for the transposed copy
+    wl(DEL, rows=48, hidden=8192),
+    wl(DEL, rows=80, hidden=2048, layout="colwise"),
+    wl(DEL, rows=112, hidden=4096, norm="layernorm", w_dtype="f32", beta_std=0.1),
 ]
 
 
