@@ -168,10 +168,18 @@ __device__ __forceinline__ void st_weight_scalar(void* base, int wdt, int64_t i,
   else reinterpret_cast<__half*>(base)[i] = __float2half_rn(v);
 }
 
-// 32-byte store (32-byte aligned): one full sector per instruction.
-__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
-  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
-               "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+// An L2 access policy that marks every line it touches evict-last.
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// 32-byte store (32-byte aligned): one full sector per instruction, under
+// the L2 cache policy `pol`.
+__device__ __forceinline__ void st_global_v8_policy(void* p, const uint32_t* w, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8}, %9;" ::"l"(p),
+               "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+               "r"(w[7]), "l"(pol)
                : "memory");
 }
 
