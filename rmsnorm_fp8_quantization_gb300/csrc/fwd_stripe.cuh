@@ -213,6 +213,8 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
       uint64_t q2[RW4];
 #pragma unroll
       for (int rr = 0; rr < RW4; ++rr) q2[rr] = 0ull;
+      // (unrolled by four: delayed scaling on 32768 x 8192 bf16 191.5 -> 189.2 us)
+#pragma unroll 4
       for (int v = lane; v < nvs; v += 32) {
 #pragma unroll
         for (int rr = 0; rr < RW4; ++rr) {
@@ -290,6 +292,9 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
         const int vl = lane & 15, rp = lane >> 4;
         const int nbands = nvs / 16;
         const int64_t sc_stride = H / 32;
+        // row steps unrolled per pass: four for RMSNorm (measured 77.8 -> 75.7 us on
+        // 16384 x 5120 bf16), two for LayerNorm (four spill there)
+        constexpr int kBandUnroll = LN ? 2 : 4;
         for (int band = warp; band < nbands; band += kStripeWarps) {
           const int v = band * 16 + vl;
           const int col = c0 + v * VEC;
@@ -334,7 +339,7 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
           uint8_t* orow = RW ? reinterpret_cast<uint8_t*>(p.out) + (i0 + rp) * H + col : nullptr;
           int64_t srow = RW && !SWZ ? (i0 + rp) * sc_stride + col / 32 : 0;
           const bool sc_lane = (v & (TPB - 1)) == 0;
-#pragma unroll 2
+#pragma unroll kBandUnroll
           for (int r = rp; r < kStripeRows; r += 4) {
             uint64_t za[NPV], zb[NPV];
             zvec(r, gw, bw, za);
@@ -412,7 +417,7 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
               }
             }
             uint8_t* crow = p.colwise_out + (i0 + rp) * H + col;
-#pragma unroll 2
+#pragma unroll kBandUnroll
             for (int r = rp; r < kStripeRows; r += 4) {
               uint64_t za[NPV], zb[NPV];
               zvec(r, gm, bm, za);
