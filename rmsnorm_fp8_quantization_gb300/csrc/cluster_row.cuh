@@ -45,6 +45,13 @@ struct RowExchange {
     return mbar_wait(&bar[k & 1], static_cast<uint32_t>((k >> 1) & 1));
   }
   __device__ const float2* entries(int64_t k) const { return &buf[(k & 1) * kMaxRowCluster]; }
+  // Zeroes the entries past C (no peer writes them), so that a merge may add
+  // all kMaxRowCluster entries without a test: adding +0 leaves a sum's bits
+  // unchanged.  Before the first cluster barrier.
+  __device__ void zero_unused(int tid, int T) const {
+    for (int i = tid; i < 2 * kMaxRowCluster; i += T)
+      if (static_cast<uint32_t>(i % kMaxRowCluster) >= C) buf[i] = make_float2(0.f, 0.f);
+  }
 };
 
 template <typename Tin, int QM, bool LN, int NV>
@@ -185,7 +192,9 @@ __global__ void __launch_bounds__(fwd_ring_max_threads(NV))
     const float2* e = ex.entries(k);
     float mean = 0.f, ss = 0.f;
     // (unrolled to the largest cluster, entries past C skipped: no loop
-    // branches per row in every thread)
+    // branches per row in every thread.  Adding all entries with zeros past C
+    // instead, as the backward does, let the loads run ahead and spill here:
+    // 4096 x 65536 bf16 LayerNorm 233 -> 347 us.)
     if constexpr (LN) {
       float msum = 0.f;
 #pragma unroll
@@ -354,6 +363,7 @@ __global__ void __launch_bounds__(bwd_max_threads(NV))
       }
     }
   }
+  ex.zero_unused(tid, T);
   cluster_sync();
 
   // slots past the warp count read as zero in the block sums; no warp writes them
@@ -448,12 +458,12 @@ __global__ void __launch_bounds__(bwd_max_threads(NV))
     {
       const float2* e = ex.entries(k);
       float tx = 0.f, ty = 0.f;
+      // (entries past C are zeros: no test per entry; 4096 x 65536 bf16
+      // LayerNorm backward 426 -> 414 us)
 #pragma unroll
       for (uint32_t c = 0; c < kMaxRowCluster; ++c) {
-        if (c < C) {
-          tx += e[c].x;
-          ty += e[c].y;
-        }
+        tx += e[c].x;
+        ty += e[c].y;
       }
       s = make_float2(tx, ty);
     }
