@@ -188,31 +188,29 @@ __global__ void __launch_bounds__(fwd_ring_max_threads(NV))
     if (tid == 0 && !ex.wait(k)) s_abort = 1;
     __syncthreads();
     if (s_abort) break;
-    // Merge in rank order (the same bits in every CTA of the cluster).
+    // Merge: lane c of every group of 8 lanes takes entry c (zero past C) and
+    // the C entries are added as a tree of xor shuffles.  Every lane, warp and
+    // CTA of the cluster adds the same pairs (fp32 addition is commutative),
+    // so all get the same bits; a warp needs no barrier and no other warp.
     const float2* e = ex.entries(k);
     float mean = 0.f, ss = 0.f;
-    // (unrolled to the largest cluster, entries past C skipped: no loop
-    // branches per row in every thread.  Adding all entries with zeros past C
-    // instead, as the backward does, let the loads run ahead and spill here:
-    // 4096 x 65536 bf16 LayerNorm 233 -> 347 us.)
-    if constexpr (LN) {
-      float msum = 0.f;
+    {
+      const uint32_t c = static_cast<uint32_t>(lane) & (kMaxRowCluster - 1);
+      const float2 v = c < C ? e[c] : make_float2(0.f, 0.f);
+      float t;
+      if constexpr (LN) {
+        float msum = v.x;
 #pragma unroll
-      for (uint32_t c = 0; c < kMaxRowCluster; ++c)
-        if (c < C) msum += e[c].x;
-      mean = msum / static_cast<float>(C);
-      const float fhc = static_cast<float>(hc);
-#pragma unroll
-      for (uint32_t c = 0; c < kMaxRowCluster; ++c) {
-        if (c < C) {
-          const float d = e[c].x - mean;
-          ss += fmaf(fhc * d, d, e[c].y);
-        }
+        for (int o = 1; o < kMaxRowCluster; o <<= 1) msum += __shfl_xor_sync(0xFFFFFFFFu, msum, o);
+        mean = msum / static_cast<float>(C);
+        const float d = v.x - mean;
+        t = c < C ? fmaf(static_cast<float>(hc) * d, d, v.y) : 0.f;
+      } else {
+        t = v.y;
       }
-    } else {
 #pragma unroll
-      for (uint32_t c = 0; c < kMaxRowCluster; ++c)
-        if (c < C) ss += e[c].y;
+      for (int o = 1; o < kMaxRowCluster; o <<= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+      ss = t;
     }
     const float rs = rsqrtf(fmaf(ss, inv_h, p.eps));
     const uint64_t rs2 = p2(rs, rs), mean2 = p2(mean, mean);
