@@ -6,8 +6,9 @@
 // its slice's statistics (forward: mean and M2, or the sum of squares;
 // backward: sum dy and sum dy*xhat) into every CTA's shared memory with
 // `st.async`, whose bytes complete a transaction count on the receiver's
-// mbarrier, and every CTA merges the C entries in rank order -- identical
-// bits in every CTA, no cluster barrier per row.
+// mbarrier, and every CTA merges the C entries the same way (forward: a tree
+// of xor shuffles over 8 lanes; backward: all 8 entries in rank order, zeros
+// past C) -- identical bits in every CTA, no cluster barrier per row.
 //
 // Operations: "Implementation:NVIDIA TransformerEngine JAX XLA
 // Normalization" (Description, I/O Contract), rowwise outputs;
