@@ -222,11 +222,19 @@ __global__ void __launch_bounds__(kSmThreads, NV == 8 ? 2 : 4)
       const int j0 = (k * gthreads + t) * V;
       words_to_floats<T, V>(w[k], u[k]);
       if (MASK != 1 && j0 + V <= limit) {  // the whole vector is kept
+        if constexpr (V >= 2) {  // two lanes per instruction
+          const uint64_t sc2 = p2(p.scale_log2e, p.scale_log2e);
 #pragma unroll
-        for (int e = 0; e < V; ++e) {
-          u[k][e] *= p.scale_log2e;
-          m = fmaxf(m, u[k][e]);
+          for (int e = 0; e < V; e += 2) {
+            const float2 f = u2(mul2(p2(u[k][e], u[k][e + 1]), sc2));
+            u[k][e] = f.x;
+            u[k][e + 1] = f.y;
+          }
+        } else {
+          u[k][0] *= p.scale_log2e;
         }
+#pragma unroll
+        for (int e = 0; e < V; ++e) m = fmaxf(m, u[k][e]);
       } else if (MASK != 1 && j0 >= limit) {
         // nothing of this vector is kept: no part in the max or the sum
       } else {
@@ -243,19 +251,30 @@ __global__ void __launch_bounds__(kSmThreads, NV == 8 ? 2 : 4)
     // nothing kept: every term is 2^-inf = 0
     const float mo = (m == -INFINITY ? 0.f : m) - 64.f;
     float s = 0.f;
+    uint64_t s2 = 0ull;  // (even, odd) partial sums, V >= 2
+    const uint64_t mo2 = p2(mo, mo);
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
       const int j0 = (k * gthreads + t) * V;
       if (MASK != 1 && j0 >= limit) {
 #pragma unroll
         for (int e = 0; e < V; ++e) u[k][e] = 0.f;
-      } else {
+      } else if constexpr (V >= 2) {
 #pragma unroll
-        for (int e = 0; e < V; ++e) {
-          u[k][e] = ex2_ftz(u[k][e] - mo);
-          s += u[k][e];
+        for (int e = 0; e < V; e += 2) {
+          const float2 d = u2(sub2(p2(u[k][e], u[k][e + 1]), mo2));
+          u[k][e] = ex2_ftz(d.x);
+          u[k][e + 1] = ex2_ftz(d.y);
+          s2 = add2(s2, p2(u[k][e], u[k][e + 1]));
         }
+      } else {
+        u[k][0] = ex2_ftz(u[k][0] - mo);
+        s += u[k][0];
       }
+    }
+    if constexpr (V >= 2) {
+      const float2 f = u2(s2);
+      s = f.x + f.y;
     }
     s = group_reduce<false>(s, buf, p.wpr);
     const float inv = s > 0.f ? 1.f / s : 0.f;
@@ -264,8 +283,17 @@ __global__ void __launch_bounds__(kSmThreads, NV == 8 ? 2 : 4)
     for (int k = 0; k < NV; ++k) {
       const int j0 = (k * gthreads + t) * V;
       if (live && j0 < sk) {
+        if constexpr (V >= 2) {
+          const uint64_t inv2 = p2(inv, inv);
 #pragma unroll
-        for (int e = 0; e < V; ++e) u[k][e] *= inv;
+          for (int e = 0; e < V; e += 2) {
+            const float2 f = u2(mul2(p2(u[k][e], u[k][e + 1]), inv2));
+            u[k][e] = f.x;
+            u[k][e + 1] = f.y;
+          }
+        } else {
+          u[k][0] *= inv;
+        }
         store_v<T, V>(yr + j0, u[k]);
       }
     }
