@@ -292,9 +292,11 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
         const int vl = lane & 15, rp = lane >> 4;
         const int nbands = nvs / 16;
         const int64_t sc_stride = H / 32;
-        // row steps unrolled per pass: four for RMSNorm (measured 77.8 -> 75.7 us on
-        // 16384 x 5120 bf16), two for LayerNorm (four spill there)
+        // row steps unrolled: RMSNorm four in pass 1, all eight in pass 2
+        // (measured on 16384 x 5120 bf16: 77.8 us with two and two, 75.7 with
+        // four and four, 73.9 with four and eight); LayerNorm two (more spill)
         constexpr int kBandUnroll = LN ? 2 : 4;
+        constexpr int kColUnroll = LN ? 2 : 8;
         for (int band = warp; band < nbands; band += kStripeWarps) {
           const int v = band * 16 + vl;
           const int col = c0 + v * VEC;
@@ -417,7 +419,7 @@ __global__ void __launch_bounds__(kStripeThreads, 3)
               }
             }
             uint8_t* crow = p.colwise_out + (i0 + rp) * H + col;
-#pragma unroll kBandUnroll
+#pragma unroll kColUnroll
             for (int r = rp; r < kStripeRows; r += 4) {
               uint64_t za[NPV], zb[NPV];
               zvec(r, gm, bm, za);
