@@ -157,6 +157,9 @@ FWD_DELAYED_CASES = [
     wl(DEL, rows=48, hidden=8192),
     wl(DEL, rows=80, hidden=2048, layout="colwise"),
     wl(DEL, rows=112, hidden=4096, norm="layernorm", w_dtype="f32", beta_std=0.1),
+    # wide rows: clusters above 8 CTAs (non-portable sizes, up to 16)
+    wl(DEL, rows=64, hidden=16384),
+    wl(DEL, rows=64, hidden=8192, in_dtype="f32", w_dtype="f32"),
 ]
 
 
@@ -183,6 +186,9 @@ FWD_MX_CASES = [
        layout="colwise"),
     wl(MX, rows=77, hidden=4096, norm="layernorm", w_dtype="f32", beta_std=0.1,
        layout="rowwise", in_dtype="f16"),
+    # wide rows: clusters above 8 CTAs (non-portable sizes, up to 16)
+    wl(MX, rows=64, hidden=16384),
+    wl(MX, rows=64, hidden=8192, in_dtype="f32", w_dtype="f32"),
 ]
 
 
