@@ -125,6 +125,10 @@ __global__ void __launch_bounds__(fwd_ring_max_threads(NV))
   int st = 0;
   uint32_t phase = 0;
   int64_t k = 0;
+  // LayerNorm with every thread holding NV full vectors and a power-of-two
+  // warp count: one block reduction per row (Chan's merge of per-thread mean
+  // and M2 over equal counts) instead of a sum, then the M2 about its mean.
+  const bool one_pass = LN && nvec == NV * T && nwarps >= 2 && (nwarps & (nwarps - 1)) == 0;
   for (; k < count; ++k, orow += row_step) {
     if (tid == 0) ex.arm(k);
     if (!mbar_wait(&full[st], phase)) s_abort = 1;
@@ -146,8 +150,52 @@ __global__ void __launch_bounds__(fwd_ring_max_threads(NV))
       const float2 a = u2(add2(acc0, acc1));
       s1 = a.x + a.y;
     }
-    if (nwarps == 1) __syncthreads();
-    s1 = row_block_sum(s1, red[rb], lane, warp, nwarps);
+    float2 mine;
+    if (LN && one_pass) {
+      // Thread: mean and M2 of its NV * VEC elements (a power of two).  Then
+      // equal halves merge as m = (m_a + m_b) / 2, M2 = M2_a + M2_b +
+      // (m_b - m_a)^2 * n / 2 (n elements per half): lanes by xor shuffles,
+      // then the warps through shared memory by the same tree, so every
+      // thread gets the same bits (each step is commutative).
+      constexpr int NE = NV * VEC;
+      const float mt = s1 * (1.f / static_cast<float>(NE));
+      const uint64_t mt2 = p2(mt, mt);
+      uint64_t q0 = 0ull, q1 = 0ull;
+#pragma unroll
+      for (int kk = 0; kk < NV; ++kk) {
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+          const uint64_t d = sub2(xp[kk][i], mt2);
+          uint64_t& q = (i & 1) ? q1 : q0;
+          q = fma2(d, d, q);
+        }
+      }
+      const float2 qq = u2(add2(q0, q1));
+      float m = mt, q = qq.x + qq.y;
+      auto merge = [](float& m, float& q, float mo, float qo, float half_n) {
+        const float d = mo - m;
+        q = (q + qo) + (d * d) * half_n;
+        m = (m + mo) * 0.5f;
+      };
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1)
+        merge(m, q, __shfl_xor_sync(0xFFFFFFFFu, m, o), __shfl_xor_sync(0xFFFFFFFFu, q, o),
+              0.5f * static_cast<float>(NE * o));
+      float2* r2 = reinterpret_cast<float2*>(red[rb]);
+      if (lane == 0) r2[warp] = make_float2(m, q);
+      __syncthreads();
+      const float2 v = r2[lane & (nwarps - 1)];
+      m = v.x;
+      q = v.y;
+      for (int o = 1; o < nwarps; o <<= 1)
+        merge(m, q, __shfl_xor_sync(0xFFFFFFFFu, m, o), __shfl_xor_sync(0xFFFFFFFFu, q, o),
+              0.5f * static_cast<float>(NE * 32 * o));
+      mine = make_float2(m, q);
+    } else {
+      if (nwarps == 1) __syncthreads();
+      s1 = row_block_sum(s1, red[rb], lane, warp, nwarps);
+      mine = make_float2(0.f, s1);
+    }
     rb ^= 1;
     if (s_abort) break;
     if (tid == 0 && issued < count) {
@@ -165,8 +213,7 @@ __global__ void __launch_bounds__(fwd_ring_max_threads(NV))
     }
     // This slice's statistics: LayerNorm (mean, M2) about the slice mean,
     // RMSNorm (0, sum of squares).
-    float2 mine = make_float2(0.f, s1);
-    if constexpr (LN) {
+    if (LN && !one_pass) {
       const float ml = s1 * inv_hc;
       const uint64_t m2 = p2(ml, ml);
       uint64_t q0 = 0ull, q1 = 0ull;
