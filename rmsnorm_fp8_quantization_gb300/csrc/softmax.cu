@@ -168,10 +168,17 @@ __global__ void __launch_bounds__(kSmThreads, NV == 8 ? 2 : 4)
   const int sk = p.sk;
   const int64_t nblocks = (p.rows + rows_per_cta - 1) / rows_per_cta;
 
+  // Index arithmetic in 32 bits when every operand fits (a 64-bit division
+  // is a long instruction sequence, taken per row).
+  const bool narrow = p.rows <= INT32_MAX && p.heads_sq <= INT32_MAX && p.mask_batches <= INT32_MAX;
+  auto mod_sq = [&](int64_t row) -> int64_t {
+    return narrow ? static_cast<int64_t>(static_cast<uint32_t>(row) % static_cast<uint32_t>(p.sq))
+                  : row % p.sq;
+  };
   // Positions j < limit of row `row` may be kept (causal rows end early).
   auto row_limit = [&](int64_t row) {
     int limit = sk;
-    const int64_t i = row % p.sq;
+    const int64_t i = mod_sq(row);
     if constexpr (MASK == 2) limit = static_cast<int>(i) + 1;
     if constexpr (MASK == 3) {
       const int64_t l = i + 1 + (sk - p.sq);
@@ -179,15 +186,21 @@ __global__ void __launch_bounds__(kSmThreads, NV == 8 ? 2 : 4)
     }
     return limit;
   };
-  auto fetch = [&](int64_t blk, uint32_t (&w)[NV][NW], uint64_t (&mb)[NV]) {
+  // Loads the block's row; `limit` is kept for compute().
+  auto fetch = [&](int64_t blk, uint32_t (&w)[NV][NW], uint64_t (&mb)[NV], int& limit) {
     const int64_t row = blk * rows_per_cta + g;
     const bool live = blk < nblocks && row < p.rows;
-    const int limit = live ? row_limit(row) : 0;
+    limit = live ? row_limit(row) : 0;
     const T* xr = reinterpret_cast<const T*>(p.x) + (live ? row : 0) * sk;
     const uint8_t* mr = nullptr;
-    if constexpr (MASK == 1)
-      mr = p.mask + ((live ? row : 0) / p.heads_sq % p.mask_batches * p.sq +
-                     (live ? row : 0) % p.sq) * static_cast<int64_t>(sk);
+    if constexpr (MASK == 1) {
+      const int64_t r = live ? row : 0;
+      const int64_t b = narrow ? static_cast<int64_t>(static_cast<uint32_t>(r) /
+                                                      static_cast<uint32_t>(p.heads_sq) %
+                                                      static_cast<uint32_t>(p.mask_batches))
+                               : r / p.heads_sq % p.mask_batches;
+      mr = p.mask + (b * p.sq + mod_sq(r)) * static_cast<int64_t>(sk);
+    }
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
       const int j0 = (k * gthreads + t) * V;
@@ -211,10 +224,10 @@ __global__ void __launch_bounds__(kSmThreads, NV == 8 ? 2 : 4)
   };
 
   // Softmax of the block's row from its packed loads w and mask bytes mb.
-  auto compute = [&](int64_t blk, const uint32_t (&w)[NV][NW], const uint64_t (&mb)[NV]) {
+  auto compute = [&](int64_t blk, const uint32_t (&w)[NV][NW], const uint64_t (&mb)[NV],
+                     const int limit) {
     const int64_t row = blk * rows_per_cta + g;
     const bool live = row < p.rows;
-    const int limit = live ? row_limit(row) : 0;
     float u[NV][V];
     float m = -INFINITY;
 #pragma unroll
@@ -301,25 +314,28 @@ __global__ void __launch_bounds__(kSmThreads, NV == 8 ? 2 : 4)
 
   uint32_t cw[NV][NW];
   uint64_t cm[NV];
+  int cl = 0;
   if constexpr (NV < 8) {
     // One block per CTA.
-    fetch(blockIdx.x, cw, cm);
-    compute(blockIdx.x, cw, cm);
+    fetch(blockIdx.x, cw, cm, cl);
+    compute(blockIdx.x, cw, cm, cl);
   } else {
     // Persistent, the next block's loads in flight during this one.
     int64_t blk = blockIdx.x;
-    fetch(blk, cw, cm);
+    fetch(blk, cw, cm, cl);
     for (; blk < nblocks; blk += gridDim.x) {
       uint32_t nw[NV][NW];
       uint64_t nm[NV];
-      fetch(blk + gridDim.x, nw, nm);
-      compute(blk, cw, cm);
+      int nl = 0;
+      fetch(blk + gridDim.x, nw, nm, nl);
+      compute(blk, cw, cm, cl);
 #pragma unroll
       for (int k = 0; k < NV; ++k) {
 #pragma unroll
         for (int e = 0; e < NW; ++e) cw[k][e] = nw[k][e];
         cm[k] = nm[k];
       }
+      cl = nl;
     }
   }
 }
