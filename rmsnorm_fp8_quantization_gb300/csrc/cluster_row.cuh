@@ -82,6 +82,8 @@ __global__ void __launch_bounds__(fwd_ring_max_threads(NV))
   const int64_t count = cid < p.rows ? (p.rows - 1 - cid) / ncl + 1 : 0;
   const int64_t row_step = ncl * H;
   const RowExchange ex{statbar, statbuf, C, rank};
+  const bool c_pow2 = (C & (C - 1)) == 0;
+  const float inv_c = 1.f / static_cast<float>(C);
   float qscale = 1.f;
   if constexpr (QM == Q_DELAYED) qscale = *p.scale;
   const uint64_t qscale2 = p2(qscale, qscale);
@@ -250,7 +252,9 @@ __global__ void __launch_bounds__(fwd_ring_max_threads(NV))
         float msum = v.x;
 #pragma unroll
         for (int o = 1; o < kMaxRowCluster; o <<= 1) msum += __shfl_xor_sync(0xFFFFFFFFu, msum, o);
-        mean = msum / static_cast<float>(C);
+        // (a multiply by 1/C where C is a power of two: the same bits, and no
+        // division sequence per row)
+        mean = c_pow2 ? msum * inv_c : msum / static_cast<float>(C);
         const float d = v.x - mean;
         t = c < C ? fmaf(static_cast<float>(hc) * d, d, v.y) : 0.f;
       } else {
