@@ -77,27 +77,6 @@ __device__ __forceinline__ void unpack(const uint32_t* w, float* f) {
   }
 }
 
-// Packs floats into words of T, round to nearest even.
-template <typename T, int N>
-__device__ __forceinline__ void pack(const float* f, uint32_t* w) {
-  if constexpr (sizeof(T) == 4) {
-#pragma unroll
-    for (int i = 0; i < N; ++i) w[i] = __float_as_uint(f[i]);
-  } else if constexpr (Elem<T>::kDt == DT_BF16) {
-#pragma unroll
-    for (int i = 0; i < N / 2; ++i) {
-      __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
-      w[i] = *reinterpret_cast<uint32_t*>(&h);
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < N / 2; ++i) {
-      __half2 h = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
-      w[i] = *reinterpret_cast<uint32_t*>(&h);
-    }
-  }
-}
-
 // Number of 32-bit words in a vector of VEC elements of T.
 template <typename T, int VEC>
 struct Words {

@@ -57,24 +57,6 @@ struct SmElem<__half> {
   static __device__ void put(__half* p, float v) { *p = __float2half_rn(v); }
 };
 
-// Loads V consecutive elements (16 bytes when V = 16 / sizeof(T)) as floats.
-template <typename T, int V>
-__device__ __forceinline__ void load_v(const T* p, float* f) {
-  if constexpr (V == 1) {
-    f[0] = SmElem<T>::get(p);
-  } else {
-    const uint4 u = ld_stream16(p);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-    uint64_t pr[V / 2];
-    widen_pairs<T, V>(w, pr);
-#pragma unroll
-    for (int i = 0; i < V / 2; ++i) {
-      const float2 t = u2(pr[i]);
-      f[2 * i] = t.x;
-      f[2 * i + 1] = t.y;
-    }
-  }
-}
 template <typename T, int V>
 __device__ __forceinline__ void store_v(T* p, const float* f) {
   if constexpr (V == 1) {
