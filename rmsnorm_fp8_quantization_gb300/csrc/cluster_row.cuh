@@ -46,11 +46,27 @@ struct RowExchange {
     return mbar_wait(&bar[k & 1], static_cast<uint32_t>((k >> 1) & 1));
   }
   __device__ const float2* entries(int64_t k) const { return &buf[(k & 1) * kMaxRowCluster]; }
-  // Zeroes the entries past C (no peer writes them), so that a merge may add
-  // all kMaxRowCluster entries without a test: adding +0 leaves a sum's bits
-  // unchanged.  Before the first cluster barrier.
-  __device__ void zero_unused(int tid, int T) const {
-    for (int i = tid; i < 2 * kMaxRowCluster; i += T)
+
+  // Two rows per exchange (pair pr): buf is [2 parities][2 rows][kMaxRowCluster].
+  __device__ void arm2(int64_t pr) const {
+    mbar_arrive_expect_tx(&bar[pr & 1], C * 2 * static_cast<uint32_t>(sizeof(float2)));
+  }
+  __device__ void push2(int64_t pr, int lane, float2 v0, float2 v1) const {
+    if (lane < static_cast<int>(C)) {
+      float2* b = &buf[(pr & 1) * 2 * kMaxRowCluster + rank];
+      push_stat(b, &bar[pr & 1], static_cast<uint32_t>(lane), v0);
+      push_stat(b + kMaxRowCluster, &bar[pr & 1], static_cast<uint32_t>(lane), v1);
+    }
+  }
+  __device__ const float2* entries2(int64_t pr, int row) const {
+    return &buf[((pr & 1) * 2 + row) * kMaxRowCluster];
+  }
+  // Zeroes the entries past C (no peer writes them) of a buffer of `n`
+  // entries, so that a merge may add all kMaxRowCluster entries without a
+  // test: adding +0 leaves a sum's bits unchanged.  Before the first cluster
+  // barrier.
+  __device__ void zero_unused(int tid, int T, int n) const {
+    for (int i = tid; i < n; i += T)
       if (static_cast<uint32_t>(i % kMaxRowCluster) >= C) buf[i] = make_float2(0.f, 0.f);
   }
 };
@@ -345,8 +361,11 @@ __global__ void __launch_bounds__(fwd_ring_max_threads(NV))
 // Backward of a long row over a cluster: a stage holds this CTA's slices of
 // dz, x (and dresidual) of one row; each CTA reduces its slice's (sum dy,
 // sum dy*xhat), the C pairs are exchanged and added in rank order, and each
-// CTA writes dx for its columns.  dgamma/dbeta partials stay in registers and
-// go to workspace row `cluster id`, columns of this CTA.
+// CTA writes dx for its columns.  Rows go two at a time through one block
+// reduction and one exchange (the exchange's round trip is the per-row cost
+// that matters here), with at least four stages so that the next two rows
+// are in flight meanwhile.  dgamma/dbeta partials stay in registers and go to
+// workspace row `cluster id`, columns of this CTA.
 template <typename Tin, bool LN, bool ADD, int NV>
 __global__ void __launch_bounds__(bwd_max_threads(NV))
     bwd_cluster_kernel(const BwdParams p, const int stages, const int hc) {
@@ -355,11 +374,10 @@ __global__ void __launch_bounds__(bwd_max_threads(NV))
   constexpr int NW = Words<Tin, VEC>::n;
   constexpr int NP = VEC / 2;
   constexpr int NS = ADD ? 3 : 2;  // slots per stage: dz, x, (dresidual)
-  constexpr bool KEEP = (NV == 1) || (NV == 2 && !LN);
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ uint64_t full[kMaxRingStages];
   __shared__ uint64_t statbar[2];
-  __shared__ float2 statbuf[2 * kMaxRowCluster];
+  __shared__ float2 statbuf[4 * kMaxRowCluster];  // [parity][row of the pair][sender]
   __shared__ __align__(16) float2 red[2][32];
   __shared__ int s_abort;
   const int tid = threadIdx.x, T = blockDim.x;
@@ -414,39 +432,38 @@ __global__ void __launch_bounds__(bwd_max_threads(NV))
       }
     }
   }
-  ex.zero_unused(tid, T);
+  ex.zero_unused(tid, T, 4 * kMaxRowCluster);
   cluster_sync();
 
-  // slots past the warp count read as zero in the block sums; no warp writes them
-  for (int i = nwarps + tid; i < 32; i += T) red[0][i] = red[1][i] = make_float2(0.f, 0.f);
-  int rb = 0;
-  int st = 0;
-  uint32_t phase = 0;
   int64_t k = 0;
-  const uint8_t* sb = ring + tid * 16;
-  Tin* dxrow = reinterpret_cast<Tin*>(p.dx) + cid * H + c0 + tid * VEC;
+  // Rows are taken in pairs (k, k + 1): one block reduction and one cluster
+  // exchange per pair, which halves the per-row exchange latency (the
+  // exchange alone costs about a quarter of the time).  Both rows are read
+  // from their stages twice (sums, then dx), so no row is held in registers
+  // across the exchange; their stages are refilled at the next pair's barrier.
+  int rb = 0;
   const int64_t vstep = static_cast<int64_t>(T) * VEC;
+  Tin* dx0 = reinterpret_cast<Tin*>(p.dx) + cid * H + c0 + tid * VEC;  // row r: + r * row_step
   const float* mup = LN ? p.mu + cid : nullptr;
   const float* rsp = p.rsigma + cid;
-  // Row statistics are loaded one row ahead so their latency is hidden.
-  float mu_next = 0.f, rs_next = 0.f;
-  if (count > 0) {
-    if constexpr (LN) mu_next = *mup;
-    rs_next = *rsp;
-  }
-  for (; k < count; ++k, dxrow += row_step) {
-    if (tid == 0) ex.arm(k);
-    const float rs = rs_next, mu = mu_next;
-    if (k + 1 < count) {
-      rsp += ncl;
-      rs_next = *rsp;
-      if constexpr (LN) {
-        mup += ncl;
-        mu_next = *mup;
-      }
+  auto row_stats = [&](int64_t r, float& mu, float& rs) {
+    rs = rsp[r * ncl];
+    mu = LN ? mup[r * ncl] : 0.f;
+  };
+  // stage and phase parity of a row, advanced row by row (no divisions)
+  auto next_stage = [&](int& s, uint32_t& ph) {
+    if (++s == stages) {
+      s = 0;
+      ph ^= 1u;
     }
-    if (!mbar_wait(&full[st], phase)) s_abort = 1;
-    uint32_t dzw[NV][NW], xw[NV][NW], rw[ADD ? NV : 1][NW];
+  };
+  int sa = 0;       // stage of row k
+  uint32_t pa = 0;  // its phase parity
+  int si = static_cast<int>(issued % stages);  // stage of the next row to issue (thread 0)
+  // this thread's dz, x (and dresidual) vectors of the row in stage s
+  auto load_row = [&](int s, uint32_t (&dzw)[NV][NW], uint32_t (&xw)[NV][NW],
+                      uint32_t (&rw)[ADD ? NV : 1][NW]) {
+    const uint8_t* sb = ring + s * stage_bytes + tid * 16;
 #pragma unroll
     for (int kk = 0; kk < NV; ++kk) {
       // No bounds test: past the slice the slots are zero, and zero dz and x
@@ -460,9 +477,12 @@ __global__ void __launch_bounds__(bwd_max_threads(NV))
         rw[kk][0] = c.x; rw[kk][1] = c.y; rw[kk][2] = c.z; rw[kk][3] = c.w;
       }
     }
-    const uint64_t mu2 = p2(mu, mu), rs2 = p2(rs, rs);
-    uint64_t sx = 0ull, sy = 0ull;  // pairs of (sum dy), (sum dy * xhat)
-    uint64_t kdy[KEEP ? NV : 1][NP], kxh[KEEP ? NV : 1][NP];
+  };
+  // (sum dy, sum dy * xhat) of the thread's part of a row; dgamma/dbeta
+  // partials accumulate
+  auto row_sums = [&](const uint32_t (&dzw)[NV][NW], const uint32_t (&xw)[NV][NW], uint64_t mu2,
+                      uint64_t rs2) {
+    uint64_t sx = 0ull, sy = 0ull;
 #pragma unroll
     for (int kk = 0; kk < NV; ++kk) {
       uint64_t fz[NP], fx[NP];
@@ -476,76 +496,32 @@ __global__ void __launch_bounds__(bwd_max_threads(NV))
         sy = fma2(dy, xh, sy);
         dg[kk][i] = fma2(fz[i], xh, dg[kk][i]);
         if constexpr (LN) db[kk][i] = add2(db[kk][i], fz[i]);
-        if constexpr (KEEP) {
-          kdy[kk][i] = dy;
-          kxh[kk][i] = xh;
-        }
       }
     }
-    float2 s;
-    {
-      const float2 a = u2(sx), b = u2(sy);
-      s = make_float2(a.x + a.y, b.x + b.y);
-    }
-    if (nwarps == 1) __syncthreads();
-    s = block_sum2(s, red[rb], lane, warp, nwarps);
-    rb ^= 1;
-    if (s_abort) break;
-    if (tid == 0 && issued < count) {
-      issue(st);
-      ++issued;
-    }
-    if (++st == stages) {
-      st = 0;
-      phase ^= 1u;
-      sb = ring + tid * 16;
-    } else {
-      sb += stage_bytes;
-    }
-    if (warp == 0) ex.push(k, lane, s);
-    // One waiter, the rest of the CTA held at the barrier (uniform exit;
-    // measured 414 vs 416 us against every thread waiting itself).
-    if (tid == 0 && !ex.wait(k)) s_abort = 1;
-    __syncthreads();
-    if (s_abort) break;
-    {
-      const float2* e = ex.entries(k);
-      float tx = 0.f, ty = 0.f;
-      // (entries past C are zeros: no test per entry; 4096 x 65536 bf16
-      // LayerNorm backward 426 -> 414 us)
-#pragma unroll
-      for (uint32_t c = 0; c < kMaxRowCluster; ++c) {
-        tx += e[c].x;
-        ty += e[c].y;
-      }
-      s = make_float2(tx, ty);
-    }
-    // dx = rs * (dy - c1 - xhat * c2) = rs * dy - rs * c1 - (rs * c2) * xhat
-    const float b1 = LN ? rs * (s.x * inv_h) : 0.f;
-    const float a2 = rs * (s.y * inv_h);
+    const float2 a = u2(sx), b = u2(sy);
+    return make_float2(a.x + a.y, b.x + b.y);
+  };
+  // dx = rs * (dy - c1 - xhat * c2) = rs * dy - rs * c1 - (rs * c2) * xhat
+  auto write_dx = [&](int64_t r, const uint32_t (&dzw)[NV][NW], const uint32_t (&xw)[NV][NW],
+                      const uint32_t (&rw)[ADD ? NV : 1][NW], float mu, float rs, float2 t) {
+    const uint64_t mu2 = p2(mu, mu), rs2 = p2(rs, rs);
+    const float b1 = LN ? rs * (t.x * inv_h) : 0.f;
+    const float a2 = rs * (t.y * inv_h);
     const uint64_t nb1 = p2(-b1, -b1), na2 = p2(-a2, -a2);
+    Tin* dxrow = dx0 + r * row_step;
 #pragma unroll
     for (int kk = 0; kk < NV; ++kk) {
       const int v = kk * T + tid;
-      uint64_t o[NP], fr[NP];
+      uint64_t o[NP], fr[NP], fz[NP], fx[NP];
       if constexpr (ADD) widen_pairs<Tin, VEC>(rw[kk], fr);
-      if constexpr (KEEP) {
+      widen_pairs<Tin, VEC>(dzw[kk], fz);
+      widen_pairs<Tin, VEC>(xw[kk], fx);
 #pragma unroll
-        for (int i = 0; i < NP; ++i) {
-          o[i] = fma2(na2, kxh[kk][i], fma2(rs2, kdy[kk][i], nb1));
-          if constexpr (ADD) o[i] = add2(o[i], fr[i]);
-        }
-      } else {
-        uint64_t fz[NP], fx[NP];
-        widen_pairs<Tin, VEC>(dzw[kk], fz);
-        widen_pairs<Tin, VEC>(xw[kk], fx);
-#pragma unroll
-        for (int i = 0; i < NP; ++i) {
-          const uint64_t xh = mul2(sub2(fx[i], mu2), rs2);
-          const uint64_t dy = mul2(fz[i], gw[kk][i]);
-          o[i] = fma2(na2, xh, fma2(rs2, dy, nb1));
-          if constexpr (ADD) o[i] = add2(o[i], fr[i]);
-        }
+      for (int i = 0; i < NP; ++i) {
+        const uint64_t xh = mul2(sub2(fx[i], mu2), rs2);
+        const uint64_t dy = mul2(fz[i], gw[kk][i]);
+        o[i] = fma2(na2, xh, fma2(rs2, dy, nb1));
+        if constexpr (ADD) o[i] = add2(o[i], fr[i]);
       }
       if (v < nvec) {
         uint32_t w[NW];
@@ -553,6 +529,75 @@ __global__ void __launch_bounds__(bwd_max_threads(NV))
         st_words<NW>(dxrow + kk * vstep, w);
       }
     }
+  };
+
+  // Row statistics are loaded one pair ahead so their latency is hidden.
+  float mu_a = 0.f, rs_a = 0.f, mu_b = 0.f, rs_b = 0.f;
+  if (count > 0) row_stats(0, mu_a, rs_a);
+  if (count > 1) row_stats(1, mu_b, rs_b);
+  for (; k < count; k += 2) {
+    const bool two = k + 1 < count;  // uniform over the cluster
+    const int64_t pr = k >> 1;       // pair index
+    if (tid == 0) ex.arm2(pr);
+    const float mua = mu_a, rsa = rs_a, mub = mu_b, rsb = rs_b;
+    if (k + 2 < count) row_stats(k + 2, mu_a, rs_a);
+    if (k + 3 < count) row_stats(k + 3, mu_b, rs_b);
+    int sb = sa;
+    uint32_t pb = pa;
+    next_stage(sb, pb);  // row k + 1
+    float2 s0, s1 = make_float2(0.f, 0.f);
+    {
+      if (!mbar_wait(&full[sa], pa)) s_abort = 1;
+      uint32_t dzw[NV][NW], xw[NV][NW], rw[ADD ? NV : 1][NW];
+      load_row(sa, dzw, xw, rw);
+      s0 = row_sums(dzw, xw, p2(mua, mua), p2(rsa, rsa));
+    }
+    if (two) {
+      if (!mbar_wait(&full[sb], pb)) s_abort = 1;
+      uint32_t dzb[NV][NW], xb[NV][NW], rwb[ADD ? NV : 1][NW];
+      load_row(sb, dzb, xb, rwb);
+      s1 = row_sums(dzb, xb, p2(mub, mub), p2(rsb, rsb));
+    }
+    const float4 s4 = block_sum4(make_float4(s0.x, s0.y, s1.x, s1.y),
+                                 reinterpret_cast<float4*>(red[rb]), lane, warp, nwarps);
+    rb ^= 1;
+    if (s_abort) break;
+    // The previous pair's rows are written: refill their stages, in row order.
+    if (tid == 0) {
+      for (; issued < count && issued < k + stages; ++issued) {
+        issue(si);
+        if (++si == stages) si = 0;
+      }
+    }
+    if (warp == 0) ex.push2(pr, lane, make_float2(s4.x, s4.y), make_float2(s4.z, s4.w));
+    // One waiter, the rest of the CTA held at the barrier (uniform exit).
+    if (tid == 0 && !ex.wait(pr)) s_abort = 1;
+    __syncthreads();
+    if (s_abort) break;
+    // entries past C are zeros: every entry is added, in rank order
+    const float2* e0 = ex.entries2(pr, 0);
+    const float2* e1 = ex.entries2(pr, 1);
+    float2 t0 = make_float2(0.f, 0.f), t1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (uint32_t c = 0; c < kMaxRowCluster; ++c) {
+      t0.x += e0[c].x;
+      t0.y += e0[c].y;
+      t1.x += e1[c].x;
+      t1.y += e1[c].y;
+    }
+    {
+      uint32_t dzw[NV][NW], xw[NV][NW], rw[ADD ? NV : 1][NW];
+      load_row(sa, dzw, xw, rw);
+      write_dx(k, dzw, xw, rw, mua, rsa, t0);
+    }
+    if (two) {
+      uint32_t dzb[NV][NW], xb[NV][NW], rwb[ADD ? NV : 1][NW];
+      load_row(sb, dzb, xb, rwb);
+      write_dx(k + 1, dzb, xb, rwb, mub, rsb, t1);
+    }
+    sa = sb;
+    pa = pb;
+    next_stage(sa, pa);
   }
 
   if (s_abort && tid == 0) {

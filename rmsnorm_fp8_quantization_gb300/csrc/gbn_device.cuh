@@ -382,6 +382,28 @@ __device__ __forceinline__ float2 block_sum2(float2 v, float2* buf, int lane, in
   return warp_sum2(r);
 }
 
+// Block-wide sum of four values (two pairs); every thread gets the same
+// bits.  `buf` holds one float4 per warp (up to 32 warps, 16-byte aligned)
+// and must alternate between two buffers on consecutive calls.  The warp
+// partials are added in warp order.
+__device__ __forceinline__ float4 block_sum4(float4 v, float4* buf, int lane, int warp,
+                                             int nwarps) {
+  const float2 a = warp_sum2(make_float2(v.x, v.y)), b = warp_sum2(make_float2(v.z, v.w));
+  v = make_float4(a.x, a.y, b.x, b.y);
+  if (nwarps == 1) return v;
+  if (lane == 0) buf[warp] = v;
+  __syncthreads();
+  float4 r = buf[0];
+  for (int w = 1; w < nwarps; ++w) {
+    const float4 u = buf[w];
+    r.x += u.x;
+    r.y += u.y;
+    r.z += u.z;
+    r.w += u.w;
+  }
+  return r;
+}
+
 // Final amax of a CTA into *amax (float bits as int: valid for values >= 0,
 // NaN compares above every finite value and Inf).  `buf` needs 32 floats and
 // must not be in use by other threads.
