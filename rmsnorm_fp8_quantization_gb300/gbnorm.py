@@ -83,20 +83,28 @@ def library():
     return _lib
 
 
+# Pointer arguments are passed as plain integers (the argtypes declare them
+# c_void_p, so ctypes converts them); None is NULL.
 def _ptr(t):
-    if t is None:
-        return None
-    if isinstance(t, int):
-        return ctypes.c_void_p(t)
-    return ctypes.c_void_p(t.data_ptr())
+    if t is None or isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+# The current stream's handle without constructing a torch.cuda.Stream
+# object (a few microseconds per call otherwise); the public call is the
+# fallback where the raw accessor is not available.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
 def _stream(stream):
     if stream is None:
-        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        if _raw_stream is not None:
+            return _raw_stream(torch.cuda.current_device())
+        return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, int):
-        return ctypes.c_void_p(stream)
-    return ctypes.c_void_p(stream.cuda_stream)
+        return stream
+    return stream.cuda_stream
 
 
 def gbn_status_string(status: int) -> str:
