@@ -442,7 +442,7 @@ def run_e2e(ops, w, inp, args, barrier, world, dev):
         sets.append((dev_in, fwd, bwd, res, host_out))
     h2d_bytes = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h_bytes = sum(t.numel() * t.element_size() for t in sets[0][4])
-    steps = max(3, args.steps // 2)
+    steps = max(3, args.steps)
 
     def h2d(b):
         for k in keys:
