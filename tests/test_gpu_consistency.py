@@ -116,7 +116,12 @@ def test_updated_amax_is_overwritten_not_merged(gpu):
     check_float("amax", out["updated_amax"], np.array([amax]), torch.float32, rel=1e-5)
 
 
-def test_cuda_graph_capture_matches_eager(gpu):
+@pytest.mark.parametrize("mode", ["current", "object", "handle"])
+def test_cuda_graph_capture_matches_eager(gpu, mode):
+    """Captured on the stream the binding is given -- the current stream
+    (stream=None), a torch stream object, or its raw handle: the outputs are
+    zeroed after the capture, so only captured kernels can write them on
+    replay."""
     w = wl("ln_bf16_16384x4096", rows=256, hidden=4096)
     inp = make_inputs(w)
     c = lambda t: t.cuda()
@@ -128,26 +133,31 @@ def test_cuda_graph_capture_matches_eager(gpu):
     db = torch.empty_like(gamma)
 
     def step():
-        gpu.norm_fwd(x, gamma, beta, norm="layernorm", eps=w.eps, outputs=o)
+        cs = torch.cuda.current_stream()
+        st = None if mode == "current" else (cs if mode == "object" else cs.cuda_stream)
+        gpu.norm_fwd(x, gamma, beta, norm="layernorm", eps=w.eps, outputs=o, stream=st)
         gpu.norm_bwd(dz, x, o["mu"], o["rsigma"], gamma, None, norm="layernorm", workspace=ws,
-                     dx=dx, dgamma=dg, dbeta=db)
+                     dx=dx, dgamma=dg, dbeta=db, stream=st)
 
+    outs = lambda: (o["out"], o["mu"], o["rsigma"], dx, dg, db)
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
         step()
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
-    eager = [t.clone() for t in (o["out"], o["mu"], o["rsigma"], dx, dg, db)]
-    for t in (o["out"], dx, dg, db):
-        t.zero_()
+    eager = [t.clone() for t in outs()]
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         step()
+    torch.cuda.synchronize()
+    for t in outs():
+        t.zero_()
+    torch.cuda.synchronize()
     for _ in range(2):
         graph.replay()
     torch.cuda.synchronize()
-    for a, b in zip(eager, (o["out"], o["mu"], o["rsigma"], dx, dg, db)):
+    for a, b in zip(eager, outs()):
         assert torch.equal(a, b)
 
 
