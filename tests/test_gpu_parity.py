@@ -128,6 +128,10 @@ FWD_NONE_CASES = [
        gamma_mean=0.0, gamma_std=0.05),
     wl(RMS1, rows=4, hidden=20000, in_dtype="bf16", w_dtype="bf16"),
     wl(RMS1, rows=2, hidden=70000, in_dtype="bf16", w_dtype="bf16"),  # beyond the vector path
+    # the widest ring rows: 6 vectors per thread (up to 384 threads), full and ragged
+    wl(LN2, rows=13, hidden=18432),
+    wl(RMS1, rows=11, hidden=17000, in_dtype="bf16", w_dtype="bf16"),
+    wl(RMS1, rows=9, hidden=9000),
 ]
 
 
@@ -160,6 +164,8 @@ FWD_DELAYED_CASES = [
     # wide rows: clusters above 8 CTAs (non-portable sizes, up to 16)
     wl(DEL, rows=64, hidden=16384),
     wl(DEL, rows=64, hidden=8192, in_dtype="f32", w_dtype="f32"),
+    # rowwise ring with 6 vectors per thread
+    wl(DEL, rows=33, hidden=18432, layout="rowwise"),
 ]
 
 
@@ -189,6 +195,8 @@ FWD_MX_CASES = [
     # wide rows: clusters above 8 CTAs (non-portable sizes, up to 16)
     wl(MX, rows=64, hidden=16384),
     wl(MX, rows=64, hidden=8192, in_dtype="f32", w_dtype="f32"),
+    # rowwise ring with 6 vectors per thread, ragged
+    wl(MX, rows=40, hidden=17408, layout="rowwise"),
 ]
 
 
@@ -211,6 +219,16 @@ BWD_CASES = [
     wl(RMS1, rows=600, hidden=256, in_dtype="bf16", w_dtype="f32"),  # many rows per CTA
     wl(RMS1, rows=3, hidden=40000, in_dtype="bf16", w_dtype="bf16"),  # beyond the vector path
     wl(RMS1, rows=1, hidden=64),
+    # rows that would need 8 vectors per thread in the ring: split over a
+    # cluster when one fits, full and ragged ...
+    wl(LN2, rows=29, hidden=16384),
+    wl(BADD, rows=23, hidden=14000),
+    wl(RMS1, rows=17, hidden=8192),
+    wl(RMS1, rows=13, hidden=7000, norm="layernorm", beta_std=0.1),
+    # ... and in the ring with 8 vectors per thread when none does
+    wl(LN2, rows=7, hidden=12296),
+    wl(BADD, rows=5, hidden=12296),
+    wl(RMS1, rows=5, hidden=7004),
 ]
 
 
