@@ -44,11 +44,11 @@
  *     least one, times the kernel's occupancy.
  *   - 1 <= hidden <= 2^24 and rows >= 0 (else GBN_ERR_SHAPE).  Rows of up to
  *     16384 two-byte (8192 four-byte) elements run on one CTA each (the
- *     backward: up to 12288 / 6144, and up to 16384 / 8192 where no cluster
- *     split fits); longer rows are split over a thread-block cluster of up to
- *     8 CTAs (forward up to 131072 / 65536 elements, backward up to 65536 /
- *     32768); longer still, or misaligned, they run on a slower generic
- *     kernel.
+ *     backward: up to 12288 / 6144, LayerNorm up to 8192 / 4096, and up to
+ *     16384 / 8192 where no cluster split fits); longer rows are split over a
+ *     thread-block cluster of up to 8 CTAs (forward up to 131072 / 65536
+ *     elements, backward up to 65536 / 32768); longer still, or misaligned,
+ *     they run on a slower generic kernel.
  *   - Norm outputs must not alias inputs.
  */
 #ifndef GBNORM_H_

@@ -229,6 +229,10 @@ BWD_CASES = [
     wl(LN2, rows=7, hidden=12296),
     wl(BADD, rows=5, hidden=12296),
     wl(RMS1, rows=5, hidden=7004),
+    # LayerNorm rows at 3 vectors per thread: over a cluster, or in the ring
+    # when no split fits
+    wl(LN2, rows=23, hidden=10240),
+    wl(LN2, rows=9, hidden=8216, dresidual=True),
 ]
 
 
