@@ -43,7 +43,7 @@
  *   - SM margin: the persistent grids use (SM count - sm_margin) SMs, at
  *     least one, times the kernel's occupancy.
  *   - 1 <= hidden <= 2^24 and rows >= 0 (else GBN_ERR_SHAPE).  Rows of up to
- *     16384 two-byte (8192 four-byte) elements run on one CTA each (the
+ *     18432 two-byte (9216 four-byte) elements run on one CTA each (the
  *     backward: up to 12288 / 6144, LayerNorm up to 8192 / 4096, and up to
  *     16384 / 8192 where no cluster split fits); longer rows are split over a
  *     thread-block cluster of up to 8 CTAs (forward up to 131072 / 65536
@@ -113,9 +113,11 @@ typedef enum {
 } gbn_status;
 
 /* Forward workspace size in bytes ("GetNormForwardWorkspaceSizes" on the
- * first page).  The forward needs no workspace, so *bytes is set to 0 for
- * every valid argument set; the call still validates its arguments.
- * Returns GBN_ERR_NULL if bytes is NULL. */
+ * first page): room for the row statistics (rsigma, and mu for LayerNorm,
+ * rounded up to 256 bytes) for columnwise FP8 layouts of rows % 32 == 0 rows
+ * longer than one CTA's ring (over 18432 two-byte / 9216 four-byte
+ * elements), 0 otherwise.  Host-only: no device is queried.  The call
+ * validates its arguments; GBN_ERR_NULL if bytes is NULL. */
 gbn_status gbn_norm_fwd_workspace_size(int64_t rows, int64_t hidden, gbn_dtype in_dtype,
                                        gbn_dtype w_dtype, gbn_dtype out_dtype,
                                        gbn_norm_type norm_type, gbn_scaling_mode scaling_mode,
@@ -149,7 +151,15 @@ gbn_status gbn_norm_fwd_workspace_size(int64_t rows, int64_t hidden, gbn_dtype i
  *   updated_amax     fp32 [1], delayed scaling: max |z| over the whole output
  *                    (before scaling; NaN propagates).  Zeroed on `stream` by
  *                    this call, then reduced into.
- *   workspace        unused (the forward needs none); may be NULL.
+ *   workspace        gbn_norm_fwd_workspace_size() bytes, 16-byte aligned, or
+ *                    NULL.  Only columnwise FP8 layouts of rows longer than
+ *                    one CTA's ring may use it: rows too long for the stripe
+ *                    kernel run the long-row kernel and then a columnwise
+ *                    tile kernel, which reads the row statistics from mu /
+ *                    rsigma or, where those are NULL, from the workspace
+ *                    (4 or, for LayerNorm, 8 bytes per row).  Without either
+ *                    such a call takes the slower generic kernel; nothing
+ *                    else reads the workspace.
  *   eps      added to the variance inside the square root.
  *
  * MXFP8 needs hidden % 32 == 0, and rows % 32 == 0 for columnwise layouts

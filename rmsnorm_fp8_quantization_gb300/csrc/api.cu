@@ -399,6 +399,21 @@ gbn_status plan_bwd(int64_t rows, int64_t hidden, gbn_dtype in, gbn_norm_type no
   return GBN_OK;
 }
 
+// Columnwise layouts of rows longer than one CTA's ring (the stripe kernel
+// may still take them, up to 16 CTAs of 2048 two-byte columns): the shapes
+// for which the forward may run the long-row kernel and then the columnwise
+// tile kernel, which needs the row statistics in memory -- in mu / rsigma, or
+// in the workspace when those are NULL.
+bool long_colwise_shape(int64_t rows, int64_t hidden, int vec) {
+  RowGeom g;
+  return rows > 0 && rows % 32 == 0 && hidden % vec == 0 &&
+         !row_geom(hidden / vec, vec, 4, fwd_ring_cap, &g);
+}
+// Workspace bytes for the row statistics: rsigma [rows] (and mu [rows]).
+size_t stats_bytes(int64_t rows, bool ln) {
+  return (static_cast<size_t>(rows) * 4u * (ln ? 2u : 1u) + 255u) / 256u * 256u;
+}
+
 }  // namespace
 
 extern "C" {
@@ -430,7 +445,11 @@ gbn_status gbn_norm_fwd_workspace_size(int64_t rows, int64_t hidden, gbn_dtype i
   const gbn_status st = check_fwd_args(rows, hidden, in_dtype, w_dtype, out_dtype, norm_type,
                                        scaling_mode, quantize_layout);
   if (st != GBN_OK) return st;
-  *bytes = 0;
+  const gbn_quantize_layout lay = base_layout(quantize_layout);
+  const bool colwise = scaling_mode != GBN_SCALING_NONE && lay != GBN_LAYOUT_ROWWISE;
+  *bytes = colwise && long_colwise_shape(rows, hidden, 16 / esize(in_dtype))
+               ? stats_bytes(rows, norm_type == GBN_LAYERNORM)
+               : 0;
   return GBN_OK;
 }
 
@@ -515,6 +534,39 @@ gbn_status gbn_norm_fwd(const void* x, const void* gamma, const void* beta, cons
       if (ncl > rows / 32) ncl = rows / 32;
       if (ncl < 1) ncl = 1;
       const cudaError_t e = kt.stripe_launch(qm, ln, sg, p, static_cast<int>(ncl), stream);
+      return e == cudaSuccess ? GBN_OK : GBN_ERR_CUDA;
+    }
+    // Rows too long for a stripe: the long-row kernel writes the row
+    // statistics, any rowwise output and the amax, then the columnwise tile
+    // kernel reads x again and writes the columnwise output from them.
+    float* smu = ln ? mu : nullptr;
+    float* srs = rsigma;
+    if (((ln && !smu) || !srs) && workspace && aligned(workspace, 16) &&
+        workspace_bytes >= stats_bytes(rows, ln)) {
+      srs = static_cast<float*>(workspace);
+      smu = ln ? srs + rows : nullptr;
+    }
+    ClusterChoice cc;
+    const int kind = qm * 2 + (ln ? 1 : 0);
+    if (vec_ok && long_colwise_shape(rows, hidden, vec) && srs && (!ln || smu) &&
+        aligned(colwise_out, qm == Q_DELAYED ? 32 : 2) &&
+        cluster_fwd_geom(kt, in_dtype, kind, qm, hidden, vec, sms, &cc)) {
+      FwdParams pa = p;
+      pa.mu = smu;
+      pa.rsigma = srs;
+      int64_t ncl = static_cast<int64_t>(static_cast<double>(cc.max_clusters) * esms / sms);
+      if (ncl > rows) ncl = rows;
+      if (ncl < 1) ncl = 1;
+      cudaError_t e = kt.fwd_cluster_launch(kind, cc.cluster, cc.threads, cc.stages,
+                                            cc.stages * cc.stage_bytes, cc.hc, pa,
+                                            static_cast<int>(ncl), stream);
+      if (e != cudaSuccess) return GBN_ERR_CUDA;
+      int occ = 0;
+      if (kt.colwise_occupancy(qm, ln, &occ) != cudaSuccess) return GBN_ERR_CUDA;
+      const int64_t tiles = rows / 32 * ((hidden + kColTileCols - 1) / kColTileCols);
+      int64_t grid = static_cast<int64_t>(esms) * (occ > 0 ? occ : 1);
+      if (grid > tiles) grid = tiles;
+      e = kt.colwise_launch(qm, ln, p, smu, srs, static_cast<int>(grid), stream);
       return e == cudaSuccess ? GBN_OK : GBN_ERR_CUDA;
     }
     vec_ok = false;  // generic kernel writes every layout

@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(fwd_ring_max_threads(NV))
           e8m0_scale(a, code, m);
           s2 = p2(m, m);
         }
-        if (act) {
+        if (act && p.write_rowwise) {  // (columnwise-only: statistics and amax only)
           uint32_t w[VEC / 4];
 #pragma unroll
           for (int i = 0; i < VEC / 4; ++i) w[i] = e4m3x4_pairs(z[2 * i], z[2 * i + 1], s2);

@@ -141,6 +141,11 @@ struct KernelTable {
   cudaError_t (*stripe_max_clusters)(int qm, bool layernorm, const StripeGeom& g, int* clusters);
   cudaError_t (*stripe_launch)(int qm, bool layernorm, const StripeGeom& g, const FwdParams& p,
                                int clusters, cudaStream_t stream);
+  // Columnwise FP8 output of rows too long for the stripe kernel, from x and
+  // row statistics written by the long-row forward before it (mu: LayerNorm).
+  cudaError_t (*colwise_occupancy)(int qm, bool layernorm, int* blocks_per_sm);
+  cudaError_t (*colwise_launch)(int qm, bool layernorm, const FwdParams& p, const float* mu,
+                                const float* rsigma, int grid, cudaStream_t stream);
   // Generic backward (any size and alignment, 256 threads).
   cudaError_t (*bwd_generic_occupancy)(int* blocks_per_sm);
   cudaError_t (*bwd_generic_launch)(const BwdParams& p, int grid, cudaStream_t stream);
@@ -174,6 +179,10 @@ struct KernelTable {
   // Sticky device-side error bits of this translation unit's kernels.
   cudaError_t (*read_device_error)(unsigned int* value, bool clear);
 };
+
+// Columnwise tile kernel: 256 threads of 2 columns, 32 rows per tile.
+constexpr int kColTileThreads = 256;
+constexpr int kColTileCols = 2 * kColTileThreads;
 
 // Vectors per thread of the long-row (cluster) kernels.
 constexpr int kClusterFwdNv = 4;

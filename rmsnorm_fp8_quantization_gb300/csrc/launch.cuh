@@ -5,6 +5,7 @@
 
 #include "bwd.cuh"
 #include "cluster_row.cuh"
+#include "fwd_colwise.cuh"
 #include "fwd_row.cuh"
 #include "fwd_stripe.cuh"
 #include "ring.cuh"
@@ -30,6 +31,25 @@ struct Launch {
     Kfwd k = fwd_generic(qm);
     if (!k) return cudaErrorInvalidValue;
     return launch_pdl(k, dim3(grid), dim3(256), 0, st, p);
+  }
+  using Kcol = void (*)(const FwdParams, const float*, const float*);
+  static Kcol colwise(int qm, bool ln) {
+    if (qm == Q_DELAYED) return ln ? fwd_colwise_kernel<Tin, Q_DELAYED, true>
+                                   : fwd_colwise_kernel<Tin, Q_DELAYED, false>;
+    if (qm == Q_MXFP8) return ln ? fwd_colwise_kernel<Tin, Q_MXFP8, true>
+                                 : fwd_colwise_kernel<Tin, Q_MXFP8, false>;
+    return nullptr;
+  }
+  static cudaError_t colwise_occupancy(int qm, bool ln, int* occ) {
+    Kcol k = colwise(qm, ln);
+    return k ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, k, kColTileThreads, 0)
+             : cudaErrorInvalidValue;
+  }
+  static cudaError_t colwise_launch(int qm, bool ln, const FwdParams& p, const float* mu,
+                                    const float* rs, int grid, cudaStream_t st) {
+    Kcol k = colwise(qm, ln);
+    if (!k) return cudaErrorInvalidValue;
+    return launch_pdl(k, dim3(grid), dim3(kColTileThreads), 0, st, p, mu, rs);
   }
   static cudaError_t bwd_generic_occupancy(int* occ) {
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, bwd_generic_kernel<Tin>, 256, 0);

@@ -70,22 +70,31 @@ def fwd_outputs(rows, hidden, in_dtype, norm="layernorm", scaling="none", layout
 
 def norm_fwd(x, gamma, beta=None, *, norm="layernorm", eps=1e-5, zero_centered_gamma=False,
              scaling="none", layout="rowwise", scale=None, amax=None, sm_margin=0,
-             training=True, outputs=None, stream=None, swizzled_scales=False):
+             training=True, outputs=None, stream=None, swizzled_scales=False, workspace=None):
     """Runs the fused forward; returns the dict of output tensors.
-    ``swizzled_scales`` (MXFP8): scales in the padded, tiled GEMM order."""
+    ``swizzled_scales`` (MXFP8): scales in the padded, tiled GEMM order.
+    ``workspace``: a uint8 device tensor of at least the queried size; allocated
+    here when the call needs one (columnwise layouts of long rows without the
+    mu / rsigma outputs)."""
     rows, hidden = x.shape
     o = outputs if outputs is not None else fwd_outputs(rows, hidden, x.dtype, norm, scaling,
                                                         layout, x.device, training,
                                                         swizzled_scales)
     in_dt = G.TORCH_DTYPE[x.dtype]
     out_dt = in_dt if scaling == "none" else G.GBN_E4M3
+    lay = _LAYOUT[layout] | (G.GBN_LAYOUT_SWIZZLED_SCALES if swizzled_scales else 0)
+    if workspace is None and (o["rsigma"] is None or (norm == "layernorm" and o["mu"] is None)):
+        st, n = G.gbn_norm_fwd_workspace_size(rows, hidden, in_dt, G.TORCH_DTYPE[gamma.dtype],
+                                              out_dt, _NORM[norm], _SCALING[scaling], lay,
+                                              zero_centered_gamma, sm_margin, training)
+        _check(st, "gbn_norm_fwd_workspace_size")
+        if n:
+            workspace = torch.empty(n, dtype=torch.uint8, device=x.device)
     st = G.gbn_norm_fwd(x, gamma, beta, scale, amax, o["out"], o["colwise_out"], o["mu"],
                         o["rsigma"], o["scale_inv"], o["colwise_scale_inv"], o["updated_amax"],
-                        None, 0, rows, hidden, in_dt, G.TORCH_DTYPE[gamma.dtype], out_dt,
-                        _NORM[norm], _SCALING[scaling],
-                        _LAYOUT[layout] | (G.GBN_LAYOUT_SWIZZLED_SCALES if swizzled_scales else 0),
-                        zero_centered_gamma,
-                        eps, sm_margin, stream)
+                        workspace, workspace.numel() if workspace is not None else 0, rows,
+                        hidden, in_dt, G.TORCH_DTYPE[gamma.dtype], out_dt, _NORM[norm],
+                        _SCALING[scaling], lay, zero_centered_gamma, eps, sm_margin, stream)
     _check(st, "gbn_norm_fwd")
     return o
 

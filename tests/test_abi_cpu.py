@@ -80,11 +80,32 @@ def test_fwd_validation_without_gpu(G):
                 **dl) == G.GBN_ERR_NULL                                      # colwise_out
 
 
-def test_fwd_workspace_size_is_zero(G):
-    st, n = G.gbn_norm_fwd_workspace_size(16384, 4096, G.GBN_BF16, G.GBN_F32, G.GBN_BF16,
-                                          G.GBN_LAYERNORM, G.GBN_SCALING_NONE,
-                                          G.GBN_LAYOUT_ROWWISE, 0, 0, 1)
-    assert st == G.GBN_OK and n == 0
+def test_fwd_workspace_size(G):
+    """Zero except for the columnwise FP8 layouts of rows longer than one CTA's
+    ring (room for rsigma, and mu for LayerNorm, rounded up to 256 bytes);
+    computed on the host, no device needed."""
+    q = lambda rows, hidden, in_dt, norm, sc, lay: G.gbn_norm_fwd_workspace_size(
+        rows, hidden, in_dt, G.GBN_BF16, G.GBN_BF16 if sc == G.GBN_SCALING_NONE else G.GBN_E4M3,
+        norm, sc, lay, 0, 0, 0)
+    assert q(16384, 4096, G.GBN_BF16, G.GBN_LAYERNORM, G.GBN_SCALING_NONE,
+             G.GBN_LAYOUT_ROWWISE) == (G.GBN_OK, 0)
+    # rows that fit one CTA's ring, or rowwise only: none
+    assert q(1024, 16384, G.GBN_BF16, G.GBN_RMSNORM, G.GBN_SCALING_DELAYED_TENSOR,
+             G.GBN_LAYOUT_ROWWISE_COLWISE) == (G.GBN_OK, 0)
+    assert q(1024, 65536, G.GBN_BF16, G.GBN_RMSNORM, G.GBN_SCALING_DELAYED_TENSOR,
+             G.GBN_LAYOUT_ROWWISE) == (G.GBN_OK, 0)
+    # long rows, columnwise: 4 bytes per row (RMSNorm), 8 (LayerNorm)
+    assert q(1024, 65536, G.GBN_BF16, G.GBN_RMSNORM, G.GBN_SCALING_DELAYED_TENSOR,
+             G.GBN_LAYOUT_COLWISE) == (G.GBN_OK, 4096)
+    assert q(96, 18464, G.GBN_BF16, G.GBN_LAYERNORM, G.GBN_SCALING_MXFP8_1D,
+             G.GBN_LAYOUT_ROWWISE_COLWISE) == (G.GBN_OK, 768)
+    assert q(64, 18432, G.GBN_BF16, G.GBN_LAYERNORM, G.GBN_SCALING_MXFP8_1D,
+             G.GBN_LAYOUT_COLWISE) == (G.GBN_OK, 0)  # the widest ring row
+    assert q(64, 9248, G.GBN_F32, G.GBN_LAYERNORM, G.GBN_SCALING_MXFP8_1D,
+             G.GBN_LAYOUT_COLWISE | G.GBN_LAYOUT_SWIZZLED_SCALES) == (G.GBN_OK, 512)
+    # ragged rows take the generic kernel: none
+    assert q(1000, 65536, G.GBN_BF16, G.GBN_RMSNORM, G.GBN_SCALING_DELAYED_TENSOR,
+             G.GBN_LAYOUT_COLWISE) == (G.GBN_OK, 0)
     st, _ = G.gbn_norm_fwd_workspace_size(16384, 4008, G.GBN_BF16, G.GBN_BF16, G.GBN_E4M3,
                                           G.GBN_RMSNORM, G.GBN_SCALING_MXFP8_1D,
                                           G.GBN_LAYOUT_ROWWISE, 0, 0, 1)

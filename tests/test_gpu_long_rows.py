@@ -36,6 +36,18 @@ FWD = [
     ("ln 131080 generic", wl("ln_bf16_16384x4096", 5, 131080)),
     ("delayed rowwise 139264 generic", wl("rms_bf16_e4m3_delayed_32768x8192", 4, 139264,
                                            layout="rowwise")),
+    # columnwise layouts of rows too long for a stripe: the long-row kernel,
+    # then the columnwise tile kernel from its statistics
+    ("delayed both 49152", wl("rms_bf16_e4m3_delayed_32768x8192", 64, 49152)),
+    ("delayed colwise ln 40960", wl("rms_bf16_e4m3_delayed_32768x8192", 32, 40960,
+                                    layout="colwise", norm="layernorm", w_dtype="f32",
+                                    beta_std=0.1)),
+    ("delayed both f32 20480", wl("rms_bf16_e4m3_delayed_32768x8192", 32, 20480,
+                                  in_dtype="f32", w_dtype="f32")),
+    ("mxfp8 both 65536", wl("rms_bf16_mxfp8_16384x5120", 32, 65536)),
+    ("mxfp8 colwise ln 36896", wl("rms_bf16_mxfp8_16384x5120", 64, 36896, layout="colwise",
+                                  norm="layernorm", w_dtype="f32", beta_std=0.1,
+                                  zero_centered_gamma=False, gamma_mean=1.0, gamma_std=0.1)),
 ]
 
 
@@ -114,3 +126,26 @@ def test_long_row_graph_capture_matches_eager(gpu):
     torch.cuda.synchronize()
     for a, b in zip(eager, (o["out"], o["rsigma"], dx, dg)):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("scaling,layout,norm", [("delayed", "rowwise_colwise", "rmsnorm"),
+                                                 ("mxfp8", "colwise", "layernorm")])
+def test_long_row_colwise_statistics_in_workspace(gpu, scaling, layout, norm):
+    """Without the mu / rsigma outputs the columnwise tile kernel reads the
+    row statistics from the workspace: every output is bit-identical to the
+    call that writes them to mu / rsigma."""
+    import torch
+    from rmsnorm_fp8_quantization_gb300.workloads import make_inputs
+    name = "rms_bf16_e4m3_delayed_32768x8192" if scaling == "delayed" else "rms_bf16_mxfp8_16384x5120"
+    w = wl(name, 64, 49152, layout=layout, norm=norm, w_dtype="f32", beta_std=0.1)
+    inp = make_inputs(w)
+    c = lambda t: None if t is None else t.cuda()
+    kw = dict(norm=norm, eps=w.eps, zero_centered_gamma=w.zero_centered_gamma, scaling=scaling,
+              layout=layout, scale=c(inp["scale"]), amax=c(inp["amax"]))
+    x, g, b = c(inp["x"]), c(inp["gamma"]), c(inp["beta"])
+    train = gpu.norm_fwd(x, g, b, training=True, **kw)
+    infer = gpu.norm_fwd(x, g, b, training=False, **kw)
+    assert infer["rsigma"] is None
+    for k, v in infer.items():
+        if v is not None:
+            assert torch.equal(v, train[k]), k
