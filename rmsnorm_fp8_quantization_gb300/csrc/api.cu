@@ -249,7 +249,13 @@ bool cluster_fwd_geom(const KernelTable& kt, int in, int kind, int qm, int64_t h
 
 // Long rows, backward: as cluster_fwd_geom with kClusterBwdNv vectors per
 // thread, at most bwd_max_threads(kClusterBwdNv) threads and 4 stages of
-// (dz, x[, dresidual]) slices.  Cached.
+// (dz, x[, dresidual]) slices.  RMSNorm takes the smallest cluster that fits;
+// LayerNorm 8 or else 4 CTAs when the CTAs keep at least 128 threads, else
+// the smallest (measured, bf16 LayerNorm backward, C = 2 against the chosen C:
+// 13088 x 10240 208 vs 163 us (C = 4; 174 at C = 5), 9344 x 14336 184 vs 168,
+// 8192 x 16384 166 vs 154, 6528 x 20480 218 vs 174 us (C = 8); RMSNorm with
+// dresidual has no such order: 8192 x 16384 189 us at C = 2, 236 at C = 4, 191
+// at C = 8).  Cached.
 bool cluster_bwd_geom(const KernelTable& kt, int in, bool ln, bool add, int64_t hidden, int vec,
                       int sms, ClusterChoice* out) {
   static std::mutex mu;
@@ -268,12 +274,16 @@ bool cluster_bwd_geom(const KernelTable& kt, int in, bool ln, bool add, int64_t 
   constexpr int64_t kTarget = 224 * 1024;
   ClusterChoice best;
   bool found = false;
-  for (int c = 2; c <= 8 && !found; ++c) {
+  // pass 0 (LayerNorm): clusters of 8, then 4, with CTAs of at least 128
+  // threads; pass 1: clusters from 2 up, any CTA size
+  for (int pass = ln ? 0 : 1; pass < 2 && !found; ++pass)
+  for (int i = 0; i < (pass == 0 ? 2 : 7) && !found; ++i) {
+    const int c = pass == 0 ? 8 >> i : 2 + i;
     if (hidden % (static_cast<int64_t>(c) * vec)) continue;
     const int64_t hc = hidden / c;
     const int64_t nvc = hc / vec;
     const int64_t t = ((nvc + kClusterBwdNv - 1) / kClusterBwdNv + 31) / 32 * 32;
-    if (t > bwd_max_threads(kClusterBwdNv)) continue;
+    if (t > bwd_max_threads(kClusterBwdNv) || (pass == 0 && t < 128)) continue;
     const int stage_bytes = (add ? 3 : 2) * ring_slot_bytes(kClusterBwdNv, static_cast<int>(t));
     int64_t best_inflight = -1;
     // at least four stages: the kernel holds the two rows of a pair while
