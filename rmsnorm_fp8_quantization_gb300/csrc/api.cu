@@ -247,15 +247,17 @@ bool cluster_fwd_geom(const KernelTable& kt, int in, int kind, int qm, int64_t h
   return found;
 }
 
-// Long rows, backward: as cluster_fwd_geom with kClusterBwdNv vectors per
-// thread, at most bwd_max_threads(kClusterBwdNv) threads and 4 stages of
-// (dz, x[, dresidual]) slices.  RMSNorm takes the smallest cluster that fits;
-// LayerNorm 8 or else 4 CTAs when the CTAs keep at least 128 threads, else
-// the smallest (measured, bf16 LayerNorm backward, C = 2 against the chosen C:
-// 13088 x 10240 208 vs 163 us (C = 4; 174 at C = 5), 9344 x 14336 184 vs 168,
-// 8192 x 16384 166 vs 154, 6528 x 20480 218 vs 174 us (C = 8); RMSNorm with
-// dresidual has no such order: 8192 x 16384 189 us at C = 2, 236 at C = 4, 191
-// at C = 8).  Cached.
+// Long rows, backward: as cluster_fwd_geom, with kClusterBwdNv vectors per
+// thread, at most bwd_max_threads(kClusterBwdNv) threads and at least 4
+// stages of (dz, x[, dresidual]) slices.  LayerNorm: over every cluster size
+// and stage count, the most bytes in flight per SM (up to the target), ties
+// to more resident CTAs; RMSNorm: the smallest cluster that fits, with its
+// stage count chosen the same way.  Measured on bf16 backward rows, smallest
+// cluster against bytes in flight: LayerNorm 13088 x 10240 208 -> 164 us,
+// 6528 x 20480 219 -> 170, 2720 x 49152 182 either way (C = 6: 512 threads on
+// 150 SMs; C = 8 would be 384 threads on the 120 SMs that 8-CTA clusters
+// reach, 225 us); RMSNorm with dresidual 7264 x 18432 211 -> 248 and 2720 x
+// 49152 207 -> 240 us, against 230 -> 215 at 20480.  Cached.
 bool cluster_bwd_geom(const KernelTable& kt, int in, bool ln, bool add, int64_t hidden, int vec,
                       int sms, ClusterChoice* out) {
   static std::mutex mu;
@@ -274,18 +276,14 @@ bool cluster_bwd_geom(const KernelTable& kt, int in, bool ln, bool add, int64_t 
   constexpr int64_t kTarget = 224 * 1024;
   ClusterChoice best;
   bool found = false;
-  // pass 0 (LayerNorm): clusters of 8, then 4, with CTAs of at least 128
-  // threads; pass 1: clusters from 2 up, any CTA size
-  for (int pass = ln ? 0 : 1; pass < 2 && !found; ++pass)
-  for (int i = 0; i < (pass == 0 ? 2 : 7) && !found; ++i) {
-    const int c = pass == 0 ? 8 >> i : 2 + i;
+  int64_t best_inflight = -1;
+  for (int c = 2; c <= 8 && (ln || !found); ++c) {
     if (hidden % (static_cast<int64_t>(c) * vec)) continue;
     const int64_t hc = hidden / c;
     const int64_t nvc = hc / vec;
     const int64_t t = ((nvc + kClusterBwdNv - 1) / kClusterBwdNv + 31) / 32 * 32;
-    if (t > bwd_max_threads(kClusterBwdNv) || (pass == 0 && t < 128)) continue;
+    if (t > bwd_max_threads(kClusterBwdNv)) continue;
     const int stage_bytes = (add ? 3 : 2) * ring_slot_bytes(kClusterBwdNv, static_cast<int>(t));
-    int64_t best_inflight = -1;
     // at least four stages: the kernel holds the two rows of a pair while
     // the next pair's rows are in flight (measured on 4096 x 65536 bf16:
     // 405 us with four, 396 with up to six or eight)
@@ -296,9 +294,10 @@ bool cluster_bwd_geom(const KernelTable& kt, int in, bool ln, bool add, int64_t 
       if (kt.bwd_cluster_max_clusters(ln, add, c, static_cast<int>(t), smem, &n) != cudaSuccess ||
           n < 1)
         continue;
-      int64_t inflight = static_cast<int64_t>(n) * c * (st > 1 ? st - 1 : 1) * stage_bytes / sms;
+      int64_t inflight = static_cast<int64_t>(n) * c * (st - 1) * stage_bytes / sms;
       if (inflight > kTarget) inflight = kTarget;
-      if (inflight > best_inflight || (inflight == best_inflight && n > best.max_clusters)) {
+      if (inflight > best_inflight ||
+          (inflight == best_inflight && n * c > best.max_clusters * best.cluster)) {
         best_inflight = inflight;
         best = ClusterChoice{c, static_cast<int>(t), static_cast<int>(hc), st, stage_bytes, n};
         found = true;
