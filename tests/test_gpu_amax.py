@@ -42,6 +42,11 @@ CASES = [
     ("cluster layernorm", wl(rows=9, hidden=24576, norm="layernorm", beta_std=0.1)),
     ("generic rms", wl(rows=17, hidden=1001)),
     ("generic layernorm", wl(rows=5, hidden=70001, norm="layernorm", beta_std=0.1)),
+    # columnwise layouts of rows too long for a stripe (the long-row kernel
+    # reduces the amax, the columnwise tile kernel writes the columns)
+    ("cluster + columnwise tiles, colwise", wl(rows=32, hidden=20480, layout="colwise")),
+    ("cluster + columnwise tiles, layernorm row+col",
+     wl(rows=64, hidden=20480, layout="rowwise_colwise", norm="layernorm", beta_std=0.1)),
 ]
 
 
@@ -51,7 +56,7 @@ def test_amax_is_max_of_the_fp32_output_run(gpu, label, w):
     c = lambda t: None if t is None else t.cuda()
     common = dict(norm=w.norm, eps=w.eps, zero_centered_gamma=w.zero_centered_gamma)
     q = gpu.norm_fwd(c(inp["x"]), c(inp["gamma"]), c(inp["beta"]), scaling="delayed",
-                     layout="rowwise", scale=c(inp["scale"]), amax=c(inp["amax"]), **common)
+                     layout=w.layout, scale=c(inp["scale"]), amax=c(inp["amax"]), **common)
     f = gpu.norm_fwd(c(inp["x"]), c(inp["gamma"]), c(inp["beta"]), **common)
     torch.cuda.synchronize()
     # the same kernel template: identical statistics

@@ -1,6 +1,6 @@
 """MXFP8 scales in the padded, tiled GEMM order (GBN_LAYOUT_SWIZZLED_SCALES):
 on every forward path (32-row stripes, the row ring, long rows over a
-cluster, the generic kernel), the codes are those of the compact call, the
+cluster, their columnwise tile kernel, the generic kernel), the codes are those of the compact call, the
 scales are the compact call's scales (checked against the oracle) placed by
 the oracle's tiling, and padding bytes are left as they were."""
 import dataclasses
@@ -28,6 +28,8 @@ CASES = [
     ("stripe colwise, 160 rows", wl(rows=160, hidden=4096, layout="colwise")),
     ("ring rowwise, ragged rows", wl(rows=130, hidden=8192, layout="rowwise")),
     ("cluster rowwise", wl(rows=33, hidden=49152, layout="rowwise")),
+    ("cluster + columnwise tiles, row+col", wl(rows=64, hidden=49152)),
+    ("cluster + columnwise tiles, colwise", wl(rows=96, hidden=36896, layout="colwise")),
     ("generic row+col", wl(rows=64, hidden=160, in_dtype="f32", norm="layernorm",
                            w_dtype="f32", beta_std=0.1)),
 ]
