@@ -192,7 +192,12 @@ RingChoice choose_ring(int key_kind, int in, const RowGeom& g, int stage_bytes, 
 // flight (up to the ring target per SM), ties to more resident CTAs.  A
 // larger cluster of smaller CTAs can win: two CTAs on an SM hide each
 // other's per-row statistics exchange (measured: 65536-wide bf16 LayerNorm
-// 312 -> 287 us with C = 8 of 256 threads instead of C = 4 of 512).  Cached.
+// 312 -> 287 us with C = 8 of 256 threads instead of C = 4 of 512).
+// LayerNorm first considers only the clusters whose CTAs take the kernel's
+// one-pass mean/M2 merge (whole vectors for every thread, a power-of-two
+// warp count of at least 2; one block reduction per row instead of two):
+// bf16 rows of 20480 123 us at C = 5 against 137 at C = 4, 28672 129 at
+// C = 7 against 144 at C = 4.  Cached.
 struct ClusterChoice {
   int cluster = 0, threads = 0, hc = 0, stages = 0, stage_bytes = 0, max_clusters = 0;
 };
@@ -216,6 +221,8 @@ bool cluster_fwd_geom(const KernelTable& kt, int in, int kind, int qm, int64_t h
   ClusterChoice best;
   bool found = false;
   int64_t best_inflight = -1;
+  const bool ln = (kind & 1) != 0;
+  for (int pass = ln ? 0 : 1; pass < 2 && !found; ++pass)
   for (int c = 2; c <= 8; ++c) {
     if (hidden % (static_cast<int64_t>(c) * vec)) continue;
     const int64_t hc = hidden / c;
@@ -223,6 +230,8 @@ bool cluster_fwd_geom(const KernelTable& kt, int in, int kind, int qm, int64_t h
     const int64_t nvc = hc / vec;
     const int64_t t = ((nvc + kClusterFwdNv - 1) / kClusterFwdNv + 31) / 32 * 32;
     if (t > fwd_ring_max_threads(kClusterFwdNv)) continue;
+    const int64_t w = t / 32;
+    if (pass == 0 && (nvc != kClusterFwdNv * t || w < 2 || (w & (w - 1)))) continue;
     const int stage_bytes = ring_slot_bytes(kClusterFwdNv, static_cast<int>(t));
     for (int st = 1; st <= kMaxRingStagesHost; ++st) {
       const int smem = st * stage_bytes;
