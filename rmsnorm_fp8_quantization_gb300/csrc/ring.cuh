@@ -167,6 +167,11 @@ __global__ void __launch_bounds__(fwd_ring_max_threads(NV)) fwd_ring_kernel(cons
   int st = 0;          // stage of row k
   uint32_t phase = 0;  // its mbarrier phase parity
   int64_t k = 0;
+  // LayerNorm with every thread holding NV full vectors and a power-of-two
+  // warp count (up to 16): one block reduction per row (a merge of per-thread
+  // mean and M2 over equal counts) instead of a sum and then the M2 about it.
+  const bool one_pass = LN && nvec == NV * T && nwarps >= 2 && nwarps <= 16 &&
+                        (nwarps & (nwarps - 1)) == 0;
   for (; k < sched.count; ++k, orow += row_step) {
     if (!mbar_wait(&full[st], phase)) s_abort = 1;
     uint64_t xp[NV][NP];
@@ -187,10 +192,55 @@ __global__ void __launch_bounds__(fwd_ring_max_threads(NV)) fwd_ring_kernel(cons
       const float2 a = u2(add2(acc0, acc1));
       s1 = a.x + a.y;
     }
-    // The barrier of the first reduction also tells thread 0 that every
-    // thread has copied its vectors out of this stage.
-    if (nwarps == 1) __syncthreads();
-    s1 = row_block_sum(s1, red[rb], lane, warp, nwarps);
+    float mean = 0.f, ss = 0.f;
+    if (LN && one_pass) {
+      // Thread: mean and M2 of its NV * VEC elements; equal halves merge as
+      // m = (m_a + m_b) / 2, M2 = M2_a + M2_b + (m_b - m_a)^2 * n / 2 (n per
+      // half), lanes by xor shuffles, then the warps through shared memory
+      // by the same tree: one block reduction per row, and every thread gets
+      // the same bits (each step is commutative).
+      constexpr int NE = NV * VEC;
+      const float mt = s1 * (1.f / static_cast<float>(NE));
+      const uint64_t mt2 = p2(mt, mt);
+      uint64_t q0 = 0ull, q1 = 0ull;
+#pragma unroll
+      for (int kk = 0; kk < NV; ++kk) {
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+          const uint64_t d = sub2(xp[kk][i], mt2);
+          uint64_t& q = (i & 1) ? q1 : q0;
+          q = fma2(d, d, q);
+        }
+      }
+      const float2 qq = u2(add2(q0, q1));
+      float m = mt, q = qq.x + qq.y;
+      auto merge = [](float& m, float& q, float mo, float qo, float half_n) {
+        const float d = mo - m;
+        q = (q + qo) + (d * d) * half_n;
+        m = (m + mo) * 0.5f;
+      };
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1)
+        merge(m, q, __shfl_xor_sync(0xFFFFFFFFu, m, o), __shfl_xor_sync(0xFFFFFFFFu, q, o),
+              0.5f * static_cast<float>(NE * o));
+      float2* r2 = reinterpret_cast<float2*>(red[rb]);
+      if (lane == 0) r2[warp] = make_float2(m, q);
+      __syncthreads();  // also: every thread has copied its vectors out of this stage
+      const float2 v = r2[lane & (nwarps - 1)];
+      m = v.x;
+      q = v.y;
+      for (int o = 1; o < nwarps; o <<= 1)
+        merge(m, q, __shfl_xor_sync(0xFFFFFFFFu, m, o), __shfl_xor_sync(0xFFFFFFFFu, q, o),
+              0.5f * static_cast<float>(NE * 32 * o));
+      mean = m;
+      ss = q;
+    } else {
+      // The barrier of the first reduction also tells thread 0 that every
+      // thread has copied its vectors out of this stage.
+      if (nwarps == 1) __syncthreads();
+      s1 = row_block_sum(s1, red[rb], lane, warp, nwarps);
+      ss = s1;
+    }
     rb ^= 1;
     if (s_abort) break;
     if (tid == 0 && issued < sched.count) {
@@ -206,8 +256,13 @@ __global__ void __launch_bounds__(fwd_ring_max_threads(NV)) fwd_ring_kernel(cons
     } else {
       xs += stage_bytes;
     }
-    float mean = 0.f, ss = s1;
-    if constexpr (LN) {
+    if (LN && one_pass) {
+      const uint64_t m2 = p2(mean, mean);
+#pragma unroll
+      for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+        for (int i = 0; i < NP; ++i) xp[kk][i] = sub2(xp[kk][i], m2);
+    } else if constexpr (LN) {
       mean = s1 * inv_h;
       const uint64_t m2 = p2(mean, mean);
       uint64_t q0 = 0ull, q1 = 0ull;
