@@ -594,8 +594,15 @@ gbn_status gbn_norm_fwd(const void* x, const void* gamma, const void* beta, cons
   if (vec_ok && row_geom(hidden / vec, vec, 4, fwd_ring_cap, &gr)) {
     // Rows streamed through a shared-memory ring by bulk copies.
     const int stage_bytes = ring_slot_bytes(gr.nv, gr.threads);
-    const int kind = qm * 2 + (ln ? 1 : 0);
-    const RingChoice rc = choose_ring(10 + kind, in_dtype, gr, stage_bytes, kMaxRingStagesHost,
+    // LayerNorm rows that fill NV = 4 vectors of every thread of a CTA of 8 or
+    // 16 warps take the one-pass mean/M2 variant (bf16 16384 x 16384: 94.1 ->
+    // 88.0 us; at 2 and 4 warps, 2048 and 4096 wide, it measured 1-4 % slower
+    // than the two-pass kernel, at 8 warps even).
+    const int warps = gr.threads / 32;
+    const bool one_pass = ln && gr.nv == 4 && hidden / vec == 4 * static_cast<int64_t>(gr.threads) &&
+                          (warps == 8 || warps == 16);
+    const int kind = qm * 2 + (ln ? 1 : 0) + (one_pass ? 6 : 0);
+    const RingChoice rc = choose_ring(30 + kind, in_dtype, gr, stage_bytes, kMaxRingStagesHost,
                                       [&](int smem, int* o) {
                                         return kt.fwd_ring_occupancy(kind, gr, smem, o);
                                       });

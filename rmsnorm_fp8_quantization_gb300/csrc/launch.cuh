@@ -129,7 +129,18 @@ struct Launch {
     }
   }
   // kind = qm * 2 + (layernorm ? 1 : 0)
+  // kinds 7, 9, 11: LayerNorm with the one-pass merge (NV = 4 only: the
+  // one geometry of the forward ring where it applies)
   static Kring fwd_ring(int kind, int nv) {
+    if (kind >= 6) {
+      if (nv != 4) return nullptr;
+      switch (kind) {
+        case 7: return fwd_ring_kernel<Tin, Q_NONE, true, 4, true>;
+        case 9: return fwd_ring_kernel<Tin, Q_DELAYED, true, 4, true>;
+        case 11: return fwd_ring_kernel<Tin, Q_MXFP8, true, 4, true>;
+        default: return nullptr;
+      }
+    }
     switch (kind) {
       case 0: return fwd_ring_for<Q_NONE, false>(nv);
       case 1: return fwd_ring_for<Q_NONE, true>(nv);

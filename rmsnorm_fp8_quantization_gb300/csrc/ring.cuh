@@ -106,9 +106,15 @@ __device__ __forceinline__ float row_block_sum(float v, float* buf, int lane, in
 // is widened to pairs once and all arithmetic runs two lanes per instruction.
 // A stage slot holds NV*T vectors; the part past the row is zero, so the
 // loads need no bounds test (zeros add nothing to either sum).
-template <typename Tin, int QM, bool LN, int NV>
+// ONE (LayerNorm only; the host selects it when every thread holds NV whole
+// vectors of the row and the CTA has 8 or 16 warps):
+// one block reduction per row, a merge of per-thread mean and M2 over equal
+// counts, instead of a sum and then the M2 about it.  A template flag, not a
+// runtime test: the two-pass variant keeps its own code.
+template <typename Tin, int QM, bool LN, int NV, bool ONE = false>
 __global__ void __launch_bounds__(fwd_ring_max_threads(NV)) fwd_ring_kernel(const FwdParams p,
                                                                            const int stages) {
+  static_assert(!ONE || LN, "the one-pass merge is LayerNorm's");
   pdl_begin();
   constexpr int VEC = 16 / (int)sizeof(Tin);
   constexpr int NW = Words<Tin, VEC>::n;
@@ -167,11 +173,6 @@ __global__ void __launch_bounds__(fwd_ring_max_threads(NV)) fwd_ring_kernel(cons
   int st = 0;          // stage of row k
   uint32_t phase = 0;  // its mbarrier phase parity
   int64_t k = 0;
-  // LayerNorm with every thread holding NV full vectors and a power-of-two
-  // warp count (up to 16): one block reduction per row (a merge of per-thread
-  // mean and M2 over equal counts) instead of a sum and then the M2 about it.
-  const bool one_pass = LN && nvec == NV * T && nwarps >= 2 && nwarps <= 16 &&
-                        (nwarps & (nwarps - 1)) == 0;
   for (; k < sched.count; ++k, orow += row_step) {
     if (!mbar_wait(&full[st], phase)) s_abort = 1;
     uint64_t xp[NV][NP];
@@ -193,7 +194,7 @@ __global__ void __launch_bounds__(fwd_ring_max_threads(NV)) fwd_ring_kernel(cons
       s1 = a.x + a.y;
     }
     float mean = 0.f, ss = 0.f;
-    if (LN && one_pass) {
+    if constexpr (ONE) {
       // Thread: mean and M2 of its NV * VEC elements; equal halves merge as
       // m = (m_a + m_b) / 2, M2 = M2_a + M2_b + (m_b - m_a)^2 * n / 2 (n per
       // half), lanes by xor shuffles, then the warps through shared memory
@@ -256,7 +257,7 @@ __global__ void __launch_bounds__(fwd_ring_max_threads(NV)) fwd_ring_kernel(cons
     } else {
       xs += stage_bytes;
     }
-    if (LN && one_pass) {
+    if constexpr (ONE) {
       const uint64_t m2 = p2(mean, mean);
 #pragma unroll
       for (int kk = 0; kk < NV; ++kk)
