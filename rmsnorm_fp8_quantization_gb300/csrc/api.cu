@@ -374,8 +374,9 @@ gbn_status plan_bwd(int64_t rows, int64_t hidden, gbn_dtype in, gbn_norm_type no
   // one fits (measured, bf16 LayerNorm 8192 x 16384: 270 vs 168 us; RMSNorm
   // with dresidual 8192 x 14000: 219 vs 172 us; fp32 8192 wide: even), and so
   // do LayerNorm rows at 3 vectors per thread, where the ring spills too
-  // (bf16 13088 x 10240: 233 vs 208 us; 10912 x 12288: 201 vs 182 us; RMSNorm
-  // there is faster in the ring: 176 vs 193 us at 12288 with dresidual).
+  // (bf16 13088 x 10240: 233 vs 162 us; 10912 x 12288: 201 vs 168 us, with
+  // the cluster size chosen below; RMSNorm there is faster in the ring: 176
+  // vs 193 us at 12288 with dresidual).
   if (g.vec != 1 && (g.nv == 8 || (ln && g.nv == 3))) {
     bool fits = true;
     for (int add = 0; add < 2; ++add) {

@@ -8,7 +8,10 @@
 // `st.async`, whose bytes complete a transaction count on the receiver's
 // mbarrier, and every CTA merges the C entries the same way (forward: a tree
 // of xor shuffles over 8 lanes; backward: all 8 entries in rank order, zeros
-// past C) -- identical bits in every CTA, no cluster barrier per row.
+// past C) -- identical bits in every CTA, no cluster barrier per row.  For
+// the columnwise FP8 layouts of such rows the forward runs first and writes
+// the statistics, the amax and any rowwise codes (none for a columnwise-only
+// layout); the columnwise tile kernel (fwd_colwise.cuh) follows.
 //
 // Operations: "Implementation:NVIDIA TransformerEngine JAX XLA
 // Normalization" (Description, I/O Contract), rowwise outputs;
